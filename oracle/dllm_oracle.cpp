@@ -1,0 +1,374 @@
+// Oracle for the parallel-decode step over one masked block.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, single-threaded CPU statement of what
+// the decode step computes.  Only the test suite, the smoke check and the benchmark's CPU-baseline
+// leg may load it; the product path never does.  It shares no code, header or constant with the
+// CUDA library: every formula below is written out directly from its definition, in double.
+//
+// Sources, cited by page title and section:
+//   dInfer explainer  = the 91haoming.cn summary of the dInfer paper (arXiv 2510.08666), with its
+//                       four components: model; diffusion-iteration manager (iteration smoothing);
+//                       decoding strategies (threshold, hierarchical, credit); KV-cache manager
+//                       (neighbourhood refresh); plus its engineering notes (early stop at EOS).
+// The pages describe each strategy in words only.  The exact formulas used here, and every
+// reading taken where the pages are silent, are stated at each function.
+//
+// Parity status: every function is pinned by the not-gpu tests (closed forms, hand-worked
+// examples, brute force, an independent second formulation, textbook GEMM).  Fidelity to the
+// dInfer code base itself is unpinned: the pages print no formula.
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <limits>
+#include <vector>
+
+namespace {
+
+const double kNegInf = -std::numeric_limits<double>::infinity();
+
+// Exact value of element i of a logits row: dtype 0 = fp32, 1 = bf16 (upper half of an fp32).
+double load_logit(const void* row, int dtype, int64_t i) {
+  if (dtype == 0) {
+    float f;
+    std::memcpy(&f, static_cast<const char*>(row) + 4 * i, 4);
+    return static_cast<double>(f);
+  }
+  uint16_t h;
+  std::memcpy(&h, static_cast<const char*>(row) + 2 * i, 2);
+  uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return static_cast<double>(f);
+}
+
+double bf16_bits_to_double(uint16_t h) {
+  uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return static_cast<double>(f);
+}
+
+// Round a non-negative finite double to the nearest bf16 value (ties to even), returned as a
+// double.  bf16 keeps 8 significant bits; normal exponents reach down to 2^-126, subnormals are
+// spaced 2^-133 apart.  Computed from the real value directly (no intermediate fp32 rounding).
+double round_to_bf16(double x) {
+  if (x == 0.0) return 0.0;
+  const double min_normal = std::ldexp(1.0, -126);
+  if (x < min_normal) {
+    return std::nearbyint(std::ldexp(x, 133)) * std::ldexp(1.0, -133);
+  }
+  int e;
+  double f = std::frexp(x, &e);          // x = f * 2^e, f in [0.5, 1)
+  double q = std::nearbyint(std::ldexp(f, 8));  // 8 significant bits, ties to even
+  return std::ldexp(q, e - 8);
+}
+
+// Index of the largest value among the masked positions, lowest index on ties; -1 if none.
+int masked_argmax(int L, const uint8_t* masked, const double* value) {
+  int best = -1;
+  for (int i = 0; i < L; ++i) {
+    if (!masked[i]) continue;
+    if (best < 0 || value[i] > value[best]) best = i;
+  }
+  return best;
+}
+
+// Apply a commit set: token <- argmax, mask cleared, committed_now set, EOS recorded.
+void apply_commits(int L, const std::vector<int>& commit, const int32_t* argmax, uint8_t* masked,
+                   int32_t* tokens, uint8_t* committed_now, int32_t* n_commit, int32_t* eos_hit,
+                   int eos_id) {
+  for (int i = 0; i < L; ++i) committed_now[i] = 0;
+  int n = 0;
+  for (int i : commit) {
+    tokens[i] = argmax[i];
+    masked[i] = 0;
+    committed_now[i] = 1;
+    ++n;
+    if (eos_id >= 0 && argmax[i] == eos_id) *eos_hit = 1;
+  }
+  *n_commit = n;
+}
+
+bool sequence_stopped(int L, const uint8_t* masked, const int32_t* eos_hit_b) {
+  if (eos_hit_b && *eos_hit_b) return true;
+  for (int i = 0; i < L; ++i)
+    if (masked[i]) return false;
+  return true;
+}
+
+// Hierarchical decoding: leaves of the recursive halving of one run [s, e).
+void halve(int s, int e, int min_width, std::vector<int>* leaves) {
+  int w = e - s;
+  if (w >= 2 * min_width) {
+    int c = s + w / 2;
+    halve(s, c, min_width, leaves);
+    halve(c, e, min_width, leaves);
+  } else {
+    leaves->push_back(s);
+    leaves->push_back(e);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// Softmax statistics of each row (dInfer explainer, decoding strategies: every strategy ranks
+// positions by the model's confidence in its top token).
+//   m = max_v z_v, s = sum_v exp(z_v - m), lse = m + ln s, conf = 1/s = exp(m - lse),
+//   argmax = lowest v attaining m.
+// Rows with active[r] == 0 are not read and report -inf, -inf, 0, -1.  active may be null.
+// logits: R rows of V elements, row r at element offset r * row_stride.
+int orc_stats(const void* logits, int dtype, int64_t R, int64_t V, int64_t row_stride,
+              const uint8_t* active, double* row_max, double* lse, double* conf,
+              int32_t* argmax) {
+  if (!logits || R < 0 || V <= 0 || row_stride < V || (dtype != 0 && dtype != 1)) return 1;
+  const int64_t esize = dtype == 0 ? 4 : 2;
+  for (int64_t r = 0; r < R; ++r) {
+    if (active && !active[r]) {
+      row_max[r] = kNegInf;
+      lse[r] = kNegInf;
+      conf[r] = 0.0;
+      argmax[r] = -1;
+      continue;
+    }
+    const void* row = static_cast<const char*>(logits) + r * row_stride * esize;
+    double m = kNegInf;
+    int64_t am = -1;
+    for (int64_t v = 0; v < V; ++v) {
+      double z = load_logit(row, dtype, v);
+      if (am < 0 || z > m) {
+        m = z;
+        am = v;
+      }
+    }
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) s += std::exp(load_logit(row, dtype, v) - m);
+    row_max[r] = m;
+    lse[r] = m + std::log(s);
+    conf[r] = 1.0 / s;
+    argmax[r] = static_cast<int32_t>(am);
+  }
+  return 0;
+}
+
+// Which rows a commit step reads: masked positions of sequences that have not stopped
+// (stopped = EOS already hit, or nothing masked; dInfer explainer, engineering notes: early stop).
+int orc_active_rows(int B, int L, const uint8_t* masked, const int32_t* eos_hit, uint8_t* active) {
+  for (int b = 0; b < B; ++b) {
+    bool stopped = eos_hit && eos_hit[b];
+    for (int i = 0; i < L; ++i) active[b * L + i] = (!stopped && masked[b * L + i]) ? 1 : 0;
+  }
+  return 0;
+}
+
+// Threshold decoding (dInfer explainer, decoding strategies, method 1: a position is fixed at
+// once when the model is confident enough in it).  Reading: commit every masked position whose
+// confidence exceeds tau (strictly); if none does, commit the single most confident masked
+// position (lowest index on ties) so that every step makes progress.
+int orc_commit_threshold(int B, int L, const double* conf, const int32_t* argmax, uint8_t* masked,
+                         int32_t* tokens, uint8_t* committed_now, int32_t* n_commit,
+                         int32_t* eos_hit, double tau, int eos_id) {
+  for (int b = 0; b < B; ++b) {
+    const double* cf = conf + b * L;
+    uint8_t* mk = masked + b * L;
+    std::vector<int> commit;
+    if (!sequence_stopped(L, mk, eos_hit + b)) {
+      for (int i = 0; i < L; ++i)
+        if (mk[i] && cf[i] > tau) commit.push_back(i);
+      if (commit.empty()) commit.push_back(masked_argmax(L, mk, cf));
+    }
+    apply_commits(L, commit, argmax + b * L, mk, tokens + b * L, committed_now + b * L,
+                  n_commit + b, eos_hit + b, eos_id);
+  }
+  return 0;
+}
+
+// Hierarchical decoding (dInfer explainer, decoding strategies, method 2: split the region still
+// to be filled recursively into smaller sub-regions and decide the centre of each first).
+// Reading: maximal masked runs are halved (cut at s + floor(w/2)) while w >= 2*min_width; in each
+// leaf the masked position closest to the leaf centre (|2i - (s+e-1)| smallest, lowest i on
+// ties) among those with conf >= tau_low is committed; a sequence that commits nothing falls
+// back to its most confident masked position.
+int orc_commit_hierarchical(int B, int L, const double* conf, const int32_t* argmax,
+                            uint8_t* masked, int32_t* tokens, uint8_t* committed_now,
+                            int32_t* n_commit, int32_t* eos_hit, double tau_low, int min_width,
+                            int eos_id) {
+  if (min_width < 1) return 1;
+  for (int b = 0; b < B; ++b) {
+    const double* cf = conf + b * L;
+    uint8_t* mk = masked + b * L;
+    std::vector<int> commit;
+    if (!sequence_stopped(L, mk, eos_hit + b)) {
+      std::vector<int> leaves;  // pairs (s, e)
+      int i = 0;
+      while (i < L) {
+        if (!mk[i]) {
+          ++i;
+          continue;
+        }
+        int s = i;
+        while (i < L && mk[i]) ++i;
+        halve(s, i, min_width, &leaves);
+      }
+      for (size_t k = 0; k < leaves.size(); k += 2) {
+        int s = leaves[k], e = leaves[k + 1];
+        int best = -1, best_dist = 0;
+        for (int j = s; j < e; ++j) {
+          if (!(cf[j] >= tau_low)) continue;
+          int dist = std::abs(2 * j - (s + e - 1));
+          if (best < 0 || dist < best_dist) {
+            best = j;
+            best_dist = dist;
+          }
+        }
+        if (best >= 0) commit.push_back(best);
+      }
+      if (commit.empty()) commit.push_back(masked_argmax(L, mk, cf));
+    }
+    apply_commits(L, commit, argmax + b * L, mk, tokens + b * L, committed_now + b * L,
+                  n_commit + b, eos_hit + b, eos_id);
+  }
+  return 0;
+}
+
+// Credit decoding (dInfer explainer, decoding strategies, method 3: every candidate token of every
+// position carries a credit that records how often and how confidently it was chosen over the
+// iterations; candidates that stay stable are boosted).  Exact rule used here, per masked
+// position with top token a and confidence p:
+//   c_k <- decay * c_k for every slot; c_a <- c_a + p (a takes the first empty slot, else evicts
+//   the slot of least credit, lowest slot on ties, and starts at p);
+//   score = p * (1 + boost * ln(1 + c_a));  commit if score > tau; fallback: largest score.
+// cand_id / cand_credit: [B, L, K]; score (nullable) receives the boosted score of active rows.
+int orc_commit_credit(int B, int L, const double* conf, const int32_t* argmax, uint8_t* masked,
+                      int32_t* tokens, uint8_t* committed_now, int32_t* n_commit,
+                      int32_t* eos_hit, int32_t* cand_id, double* cand_credit, int K,
+                      double decay, double boost, double tau, int eos_id, double* score_out) {
+  if (K < 1) return 1;
+  std::vector<double> score(L);
+  for (int b = 0; b < B; ++b) {
+    const double* cf = conf + b * L;
+    uint8_t* mk = masked + b * L;
+    std::vector<int> commit;
+    if (!sequence_stopped(L, mk, eos_hit + b)) {
+      for (int i = 0; i < L; ++i) {
+        score[i] = 0.0;
+        if (!mk[i]) continue;
+        int32_t* ids = cand_id + (static_cast<int64_t>(b) * L + i) * K;
+        double* cr = cand_credit + (static_cast<int64_t>(b) * L + i) * K;
+        const int32_t a = argmax[b * L + i];
+        const double p = cf[i];
+        for (int k = 0; k < K; ++k) cr[k] = decay * cr[k];
+        int slot = -1;
+        for (int k = 0; k < K; ++k)
+          if (ids[k] == a) slot = k;
+        if (slot >= 0) {
+          cr[slot] += p;
+        } else {
+          for (int k = 0; k < K && slot < 0; ++k)
+            if (ids[k] == -1) slot = k;
+          if (slot < 0) {
+            slot = 0;
+            for (int k = 1; k < K; ++k)
+              if (cr[k] < cr[slot]) slot = k;
+          }
+          ids[slot] = a;
+          cr[slot] = p;
+        }
+        score[i] = p * (1.0 + boost * std::log1p(cr[slot]));
+      }
+      for (int i = 0; i < L; ++i)
+        if (mk[i] && score[i] > tau) commit.push_back(i);
+      if (commit.empty()) commit.push_back(masked_argmax(L, mk, score.data()));
+      if (score_out)
+        for (int i = 0; i < L; ++i) score_out[b * L + i] = mk[i] ? score[i] : 0.0;
+    } else if (score_out) {
+      for (int i = 0; i < L; ++i) score_out[b * L + i] = 0.0;
+    }
+    apply_commits(L, commit, argmax + b * L, mk, tokens + b * L, committed_now + b * L,
+                  n_commit + b, eos_hit + b, eos_id);
+  }
+  return 0;
+}
+
+// Rows that iteration smoothing carries into the next round: still masked after the commit, in
+// sequences that have not stopped, listed in ascending row order (dInfer explainer, diffusion-
+// iteration manager: undecided positions keep their distribution instead of dropping it).
+int orc_smooth_rows(int B, int L, const uint8_t* masked, const int32_t* eos_hit, int32_t* row_ids,
+                    int32_t* M) {
+  int n = 0;
+  for (int b = 0; b < B; ++b) {
+    if (eos_hit && eos_hit[b]) continue;
+    for (int i = 0; i < L; ++i)
+      if (masked[b * L + i]) row_ids[n++] = b * L + i;
+  }
+  *M = n;
+  return 0;
+}
+
+// Soft input embedding of one smoothed row (dInfer explainer, diffusion-iteration manager,
+// iteration smoothing): the row's probabilities, each rounded to bf16 (nearest even), weight the
+// rows of the embedding table.  S[j, c] = sum_v bf16(exp(z_v - lse)) * E[v, c].
+// E: bf16 bit patterns [V, d] row-major.  out: [M, d].
+int orc_smooth_embed(const void* logits, int dtype, int64_t V, int64_t row_stride,
+                     const double* lse, const int32_t* row_ids, int64_t M, const uint16_t* E,
+                     int64_t d, double* out) {
+  const int64_t esize = dtype == 0 ? 4 : 2;
+  std::vector<double> acc(d);
+  for (int64_t j = 0; j < M; ++j) {
+    const int64_t r = row_ids[j];
+    const void* row = static_cast<const char*>(logits) + r * row_stride * esize;
+    for (int64_t c = 0; c < d; ++c) acc[c] = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+      double p = round_to_bf16(std::exp(load_logit(row, dtype, v) - lse[r]));
+      if (p == 0.0) continue;
+      const uint16_t* e = E + v * d;
+      for (int64_t c = 0; c < d; ++c) acc[c] += p * bf16_bits_to_double(e[c]);
+    }
+    for (int64_t c = 0; c < d; ++c) out[j * d + c] = acc[c];
+  }
+  return 0;
+}
+
+// The bf16 probability row itself (for checking the materialised operand).
+int orc_prob_row_bf16(const void* logits, int dtype, int64_t V, int64_t row_stride, int64_t r,
+                      double lse_r, double* p) {
+  const int64_t esize = dtype == 0 ? 4 : 2;
+  const void* row = static_cast<const char*>(logits) + r * row_stride * esize;
+  for (int64_t v = 0; v < V; ++v) p[v] = round_to_bf16(std::exp(load_logit(row, dtype, v) - lse_r));
+  return 0;
+}
+
+int orc_round_to_bf16(const double* x, int64_t n, double* y) {
+  for (int64_t i = 0; i < n; ++i) y[i] = round_to_bf16(x[i]);
+  return 0;
+}
+
+// Neighbourhood KV refresh (dInfer explainer, KV-cache manager: when a region changes, its cache
+// entries and those of its neighbours are recomputed).  Cache row = [prefix 0..P)[block P..P+L);
+// refresh[j] = 1 iff a position i committed in this step has |j - (P + i)| <= window.
+// idx lists the refreshed j ascending, then -1; count = number refreshed.
+int orc_kv_refresh(int B, int L, const uint8_t* committed_now, int prefix_len, int window,
+                   uint8_t* refresh, int32_t* idx, int32_t* count) {
+  if (prefix_len < 0 || window < 0) return 1;
+  const int T = prefix_len + L;
+  for (int b = 0; b < B; ++b) {
+    int n = 0;
+    for (int j = 0; j < T; ++j) {
+      uint8_t hit = 0;
+      for (int i = 0; i < L; ++i) {
+        if (!committed_now[b * L + i]) continue;
+        if (std::abs(j - (prefix_len + i)) <= window) hit = 1;
+      }
+      refresh[static_cast<int64_t>(b) * T + j] = hit;
+      if (hit) idx[static_cast<int64_t>(b) * T + n++] = j;
+    }
+    for (int k = n; k < T; ++k) idx[static_cast<int64_t>(b) * T + k] = -1;
+    count[b] = n;
+  }
+  return 0;
+}
+
+}  // extern "C"
