@@ -1,0 +1,510 @@
+#!/usr/bin/env python3
+"""Benchmark of the parallel-decode step on GB300.
+
+One step = one full decode iteration over a batch of blocks: the fused softmax-statistics +
+threshold-commit kernel, the smoothing probability rows, the tcgen05 smoothing GEMM and the
+KV-refresh mask (workload "smooth_step": B=16 blocks of L=64 positions, V=126464, d=2048).
+Other workloads (--workload threshold_loop | hierarchical_loop | credit_loop |
+threshold_single) time the decode loops instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload smooth_step]
+
+Prints ONE JSON line (rank 0).  With N > 1 (torchrun), every rank runs its own independent
+batch (weak scaling, no collective on the data path); value = all ranks' block-iterations over
+the slowest rank's time.  --impl reference times the oracle (plain single-threaded C++) on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+from synth.workloads import SEEDS, WORKLOADS  # noqa: E402
+
+METRIC = "decode iters/s per block; logit GB/s as fraction of GB300 HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------ environment helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            v = d.get(k)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[k] = float(v) if v is not None else FALLBACK_PEAKS[k]
+        return out, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank decodes its own batch (independent problems: weak scaling)."""
+    return base + 7919 * rank
+
+
+# ------------------------------------------------------------------ our arm: smooth_step
+
+def algorithmic_bytes_stats(w, rows_read: int) -> int:
+    """Logit bytes one stats launch must read (masked rows only) + state/stat writes."""
+    es = 2 if w.dtype == "bf16" else 4
+    return rows_read * w.V * es
+
+
+def run_smooth_step(args, rank, world, local):
+    import diffusion_decoding_gb300 as dd
+
+    w = WORKLOADS["smooth_step"]
+    dev = torch.device("cuda", local)
+    seed = rank_seed(SEEDS[w.key], rank)
+    B, L, V, d = w.B, w.L, w.V, w.d
+    R = B * L
+    T = w.prefix_len + L
+    lg_host = synth.logits(w, seed)                       # uint16 bf16 bits [B, L, V]
+    E_host = synth.embedding_table(seed + 1, V, d)        # uint16 bf16 bits [V, d]
+    logits = torch.from_numpy(lg_host.view(np.int16)).view(torch.bfloat16).to(dev)
+    E = torch.from_numpy(E_host.view(np.int16)).to(dev)
+    Et = torch.empty(dd.dllm_embedding_t_elems(V, d), dtype=torch.int16, device=dev)
+    dd.dllm_prepare_embedding(E, Et)
+    del E
+    shape = dd.make_shape(B, L, V, dd.DLLM_BF16)
+    state = dd.BlockState(B, L, device=dev)
+    fresh = dd.BlockState(B, L, device=dev)
+    stats = dd.StatsBuffers(R, device=dev)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape), dev)
+    ws_s = dd.workspace(dd.dllm_smooth_workspace_bytes(shape, d), dev)
+    out = torch.empty(R, d, dtype=torch.float32, device=dev)
+    row_ids = torch.empty(R, dtype=torch.int32, device=dev)
+    M = torch.zeros(1, dtype=torch.int32, device=dev)
+    refresh = torch.empty(B * T, dtype=torch.uint8, device=dev)
+    idx = torch.empty(B * T, dtype=torch.int32, device=dev)
+    count = torch.empty(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def reset_state():
+        for name in ("masked", "tokens", "committed_now", "n_commit", "eos_hit"):
+            getattr(state, name).copy_(getattr(fresh, name), non_blocking=True)
+
+    ev = {}
+
+    def step(lg, timed=False):
+        reset_state()
+        if timed:
+            ev["a0"].record(stream)
+        dd.dllm_commit_threshold(lg, shape, stats, state, w.tau, w.eos_id, ws)
+        if timed:
+            ev["a1"].record(stream)
+        dd.dllm_smooth_probs(lg, shape, stats, state, d, row_ids, M, ws_s)
+        if timed:
+            ev["b0"].record(stream)
+        dd.dllm_smooth_gemm(shape, Et, d, out, M, ws_s)
+        if timed:
+            ev["b1"].record(stream)
+        dd.dllm_kv_refresh_mask(state, w.prefix_len, w.window, refresh, idx, count)
+
+    for _ in range(args.warmup):
+        step(logits)
+    torch.cuda.synchronize(dev)
+    Mv = int(M.item())
+
+    # per-kernel timing (events on the launching stream), then the whole-step timing
+    t_stats, t_gemm, t_prob = [], [], []
+    for _ in range(args.steps):
+        ev.update({k: torch.cuda.Event(enable_timing=True) for k in ("a0", "a1", "b0", "b1")})
+        step(logits, timed=True)
+        torch.cuda.synchronize(dev)
+        t_stats.append(ev["a0"].elapsed_time(ev["a1"]))
+        t_prob.append(ev["a1"].elapsed_time(ev["b0"]))
+        t_gemm.append(ev["b0"].elapsed_time(ev["b1"]))
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(logits)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, world)
+    assert dd.dllm_get_status(ws_s) == dd.DLLM_OK
+
+    # end to end through the public API with host buffers: H2D logits, step, D2H results
+    lg_pin = torch.from_numpy(lg_host.view(np.int16)).pin_memory()
+    lg_dev = torch.empty(B, L, V, dtype=torch.int16, device=dev)
+    res_dev = [state.tokens, state.masked, state.n_commit, row_ids, M, out, idx, count]
+    res_pin = [torch.empty_like(t, device="cpu").pin_memory() for t in res_dev]
+    h2d = lg_pin.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in res_dev)
+
+    def e2e_step():
+        lg_dev.copy_(lg_pin, non_blocking=True)
+        step(lg_dev.view(torch.bfloat16))
+        for hp, dv in zip(res_pin, res_dev):
+            hp.copy_(dv, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
+
+    peaks, peak_src = load_peaks()
+    gemm_ms = statistics.mean(t_gemm)
+    stats_ms = statistics.mean(t_stats)
+    prob_ms = statistics.mean(t_prob)
+    flops = 2.0 * Mv * V * d
+    gemm_tf = flops / (gemm_ms * 1e-3) / 1e12
+    stats_bytes = algorithmic_bytes_stats(w, R)
+    stats_gbs = stats_bytes / (stats_ms * 1e-3) / 1e9
+    prob_bytes = Mv * V * 2 * 2  # read logits rows + write bf16 P rows
+    prob_gbs = prob_bytes / (prob_ms * 1e-3) / 1e9
+    step_bytes = R * V * 2
+    plan = dd.dllm_smooth_plan_info(shape, d)
+    launches_per_step = 1 + plan["launches"] + 1  # commit, smoothing kernels, refresh
+    res = {
+        "metric": METRIC,
+        "value": world * B * 1e3 / ms,
+        "unit": "block-iters/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,2) bf16 logits, N(0,0.02) bf16 embedding table)",
+        "config": {"workload": "smooth_step: threshold commit (tau 0.9) + iteration smoothing "
+                               "(softmax x E, d=2048) + KV refresh (prefix 1024, window 4)",
+                   "B": B, "L_block": L, "V": V, "d": d, "M_smoothed": Mv, "gemm_plan": plan,
+                   "l2": "inputs larger than L2 (259 MB logits + 518 MB table per step)",
+                   "parallelism": f"replicas x{world}"},
+        "iters_per_s": 1e3 / ms,
+        "logit_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "tensor", "kernel": "smooth_gemm_kernel", "achieved": gemm_tf,
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": gemm_tf / peaks["bf16_tflops_sustained"],
+                     "peak_source": f"{peak_src} bf16 sustained",
+                     "frac_of_burst": gemm_tf / peaks["bf16_tflops"],
+                     "traffic": None, "ms": gemm_ms,
+                     "algorithmic": f"2*M*V*d = {flops:.4g} FLOP per launch"},
+        "roofline_stats": {"bound": "hbm", "kernel": "stats_commit_kernel", "achieved": stats_gbs,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": stats_gbs / peaks["hbm_gbs"], "frac_of_8tbs": stats_gbs / 8000,
+                           "peak_source": f"{peak_src} HBM copy", "traffic": None,
+                           "ms": stats_ms,
+                           "algorithmic": f"{stats_bytes} logit bytes per launch"},
+        "roofline_probs": {"bound": "hbm", "kernel": "prob_rows_kernel", "achieved": prob_gbs,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": prob_gbs / peaks["hbm_gbs"], "ms": prob_ms},
+        "e2e": {"value": world * B * 1e3 / ms_e2e, "unit": "block-iters/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    return res
+
+
+# ------------------------------------------------------------------ our arm: decode loops
+
+def run_loop(args, rank, world, local, key):
+    import diffusion_decoding_gb300 as dd
+
+    w = WORKLOADS[key]
+    dev = torch.device("cuda", local)
+    seed = rank_seed(SEEDS[key], rank)
+    n_it = w.max_iters
+    # pre-generate every iteration's logits in HBM (the generator is outside the timed region)
+    lgs = [torch.from_numpy(synth.logits(w, seed, it).view(np.int16 if w.dtype == "bf16"
+                                                            else np.float32)).to(dev)
+           for it in range(n_it)]
+    if w.dtype == "bf16":
+        lgs = [t.view(torch.bfloat16) for t in lgs]
+    shape = dd.make_shape(w.B, w.L, w.V, dd.DLLM_BF16 if w.dtype == "bf16" else dd.DLLM_F32)
+    state = dd.BlockState(w.B, w.L, w.K, device=dev)
+    stats = dd.StatsBuffers(w.B * w.L, device=dev)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(lg):
+        if w.strategy == "threshold":
+            dd.dllm_commit_threshold(lg, shape, stats, state, w.tau, w.eos_id, ws)
+        elif w.strategy == "hierarchical":
+            dd.dllm_commit_hierarchical(lg, shape, stats, state, w.tau_low, w.min_width,
+                                        w.eos_id, ws)
+        else:
+            dd.dllm_commit_credit(lg, shape, stats, state, w.K, w.decay, w.boost, w.tau,
+                                  w.eos_id, ws)
+
+    def loop():
+        state.reset()
+        for lg in lgs:
+            one(lg)
+
+    for _ in range(args.warmup):
+        loop()
+    torch.cuda.synchronize(dev)
+    # rows actually read per iteration (masked rows of running sequences), for GB/s
+    rows = []
+    state.reset()
+    for lg in lgs:
+        m = state.masked.view(w.B, w.L).clone()
+        e = state.eos_hit.clone()
+        rows.append(int((m.sum(1) * (e == 0)).sum().item()))
+        one(lg)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        loop()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms_loop = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    # first (fully masked) iteration alone, L2 flushed before each launch
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    t1 = []
+    for _ in range(args.steps):
+        state.reset()
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one(lgs[0])
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        t1.append(a.elapsed_time(b))
+    peaks, peak_src = load_peaks()
+    es = 2 if w.dtype == "bf16" else 4
+    ms1 = statistics.median(t1)
+    gbs1 = rows[0] * w.V * es / (ms1 * 1e-3) / 1e9
+    total_bytes = sum(rows) * w.V * es
+    return {
+        "metric": METRIC,
+        "value": world * w.B * n_it * 1e3 / ms_loop,
+        "unit": "block-iters/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_loop, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded planted-peak logits)",
+        "config": {"workload": f"{key}: {w.title}", "iterations_per_step": n_it,
+                   "l2": "per-iteration logits pre-generated in HBM and rotated; "
+                         "single-iteration timing flushes L2 first"},
+        "iters_per_s": n_it * 1e3 / ms_loop,
+        "loop_logit_gbs": total_bytes / (ms_loop * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "stats_commit_kernel", "achieved": gbs1,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs1 / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} HBM copy", "traffic": None, "ms": ms1,
+                     "algorithmic": f"{rows[0]} rows x V x {es} B"},
+        "gpu_launches": n_it * args.steps,
+        "clocks": clk,
+    }
+
+
+# ------------------------------------------------------------------ reference arm: the oracle
+
+def cpu_sample_smooth(seed: int, smooth_rows: int):
+    """Time the oracle on a bounded sample of smooth_step; returns (seconds per full step, info)."""
+    import oracle
+
+    w = WORKLOADS["smooth_step"]
+    lg = synth.logits(w, seed)
+    E = synth.embedding_table(seed + 1, w.V, w.d)
+    st = oracle.BlockState(w.B, w.L)
+    t0 = time.perf_counter()
+    s = oracle.stats(lg, oracle.active_rows(st.masked, st.eos_hit))
+    oracle.commit_threshold(st, s.conf.reshape(w.B, w.L), s.argmax.reshape(w.B, w.L),
+                            float(np.float32(w.tau)), w.eos_id)
+    ids = oracle.smooth_rows(st.masked, st.eos_hit)
+    oracle.kv_refresh(st.committed_now, w.prefix_len, w.window)
+    t_commit = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.smooth_embed(lg.reshape(-1, w.V), s.lse, ids[:smooth_rows], E)
+    t_rows = time.perf_counter() - t0
+    per_row = t_rows / smooth_rows
+    est = t_commit + per_row * len(ids)
+    info = (f"oracle, 1 thread: stats+commit+refresh over all {w.B * w.L} rows "
+            f"({t_commit:.2f} s) + smoothing of {smooth_rows} of {len(ids)} rows "
+            f"({per_row:.3f} s/row), extrapolated to the full step ({est:.1f} s)")
+    return est, info
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    key = args.workload
+    if key != "smooth_step":
+        return {"impl": "reference", "unavailable": "reference arm implemented for smooth_step"}
+    times, info = [], ""
+    for i in range(args.warmup + args.steps):
+        est, info = cpu_sample_smooth(SEEDS[key], smooth_rows=1)
+        if i >= args.warmup:
+            times.append(est)
+    w = WORKLOADS[key]
+    sec = statistics.mean(times)
+    value = w.B / sec
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "block-iters/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": key, "B": w.B, "L_block": w.L, "V": w.V,
+                                        "d": w.d},
+        "cpu_baseline": {"value": value, "unit": "block-iters/s", "cores": 1, "kind": "oracle",
+                         "sample": info},
+        "e2e": {"value": value, "unit": "block-iters/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="smooth_step", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    from diffusion_decoding_gb300 import build as cuda_build
+    cuda_build.build()
+    if args.workload == "smooth_step":
+        res = run_smooth_step(args, rank, world, local)
+    else:
+        res = run_loop(args, rank, world, local, args.workload)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline and args.workload == "smooth_step":
+            import multiprocessing
+            est, info = cpu_sample_smooth(SEEDS[args.workload], smooth_rows=8)
+            res["cpu_baseline"] = {"value": WORKLOADS[args.workload].B / est,
+                                   "unit": "block-iters/s", "cores": 1, "kind": "oracle",
+                                   "sample": info,
+                                   "host_cores": multiprocessing.cpu_count()}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

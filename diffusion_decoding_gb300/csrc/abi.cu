@@ -1,0 +1,323 @@
+// C ABI of the decode step: argument validation, workspace layout and kernel launches.
+// Every entry point validates on the host first and launches nothing when it returns an error.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_err[512];
+
+dllm_status fail(dllm_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+dllm_status ok() {
+  g_err[0] = '\0';
+  return DLLM_OK;
+}
+
+dllm_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(DLLM_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+dllm_status check_shape(const dllm_shape* sh) {
+  if (!sh) return fail(DLLM_ERR_INVALID_ARG, "shape is null");
+  if (sh->B < 1 || sh->L < 1 || sh->V < 1)
+    return fail(DLLM_ERR_INVALID_ARG, "B, L and V must be positive (B=%d L=%d V=%d)", sh->B,
+                sh->L, sh->V);
+  if (sh->dtype != DLLM_F32 && sh->dtype != DLLM_BF16)
+    return fail(DLLM_ERR_UNSUPPORTED, "dtype %d is not fp32 (0) or bf16 (1)", sh->dtype);
+  if (sh->L > dllm::kMaxL) return fail(DLLM_ERR_UNSUPPORTED, "L=%d exceeds %d", sh->L, dllm::kMaxL);
+  if (static_cast<int64_t>(sh->B) * sh->L > (int64_t{1} << 20))
+    return fail(DLLM_ERR_UNSUPPORTED, "B*L=%lld exceeds 2^20",
+                static_cast<long long>(sh->B) * sh->L);
+  if (sh->row_stride < sh->V)
+    return fail(DLLM_ERR_INVALID_ARG, "row_stride %lld < V %d",
+                static_cast<long long>(sh->row_stride), sh->V);
+  const int es = sh->dtype == DLLM_BF16 ? 2 : 4;
+  if ((sh->row_stride * es) % 16 != 0)
+    return fail(DLLM_ERR_INVALID_ARG, "row_stride*element size must be a multiple of 16 bytes");
+  return DLLM_OK;
+}
+
+dllm_status check_ws(const void* ws) {
+  if (!ws) return fail(DLLM_ERR_INVALID_ARG, "workspace is null");
+  if (!aligned(ws, 256)) return fail(DLLM_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  return DLLM_OK;
+}
+
+dllm_status check_stats(const dllm_stats* st) {
+  if (!st || !st->row_max || !st->lse || !st->conf || !st->argmax)
+    return fail(DLLM_ERR_INVALID_ARG, "stats or one of its arrays is null");
+  return DLLM_OK;
+}
+
+dllm_status check_state(const dllm_block_state* s) {
+  if (!s || !s->masked || !s->tokens || !s->committed_now || !s->n_commit || !s->eos_hit)
+    return fail(DLLM_ERR_INVALID_ARG, "block state or one of its arrays is null");
+  return DLLM_OK;
+}
+
+dllm_status check_logits(const void* logits) {
+  if (!aligned(logits, 16)) return fail(DLLM_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+  return DLLM_OK;
+}
+
+#define DLLM_TRY(x)                 \
+  do {                              \
+    dllm_status s_ = (x);           \
+    if (s_ != DLLM_OK) return s_;   \
+  } while (0)
+
+// Shared body of the three commit entry points.
+dllm_status commit_common(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
+                          const dllm_block_state* state, const dllm::CommitArgs& ca, void* ws,
+                          dllm_stream_t stream, const char* name) {
+  DLLM_TRY(check_shape(shape));
+  DLLM_TRY(check_stats(stats));
+  DLLM_TRY(check_state(state));
+  cudaError_t e;
+  if (logits) {
+    DLLM_TRY(check_logits(logits));
+    DLLM_TRY(check_ws(ws));
+    const dllm::StatsWs w = dllm::stats_ws_layout(ws, shape->B, shape->L, shape->V);
+    e = dllm::launch_stats_commit(logits, *shape, nullptr, *stats, state, ca, w, sm_count(),
+                                  reinterpret_cast<cudaStream_t>(stream));
+  } else {
+    e = dllm::launch_commit_only(*shape, *stats, *state, ca,
+                                 reinterpret_cast<cudaStream_t>(stream));
+  }
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dllm_last_error(void) { return g_err; }
+
+size_t dllm_workspace_bytes(const dllm_shape* shape) {
+  if (check_shape(shape) != DLLM_OK) return 0;
+  return dllm::stats_ws_bytes(shape->B, shape->L, shape->V);
+}
+
+dllm_status dllm_decode_stats(const void* logits, const dllm_shape* shape, const uint8_t* masked,
+                              const dllm_stats* out, void* ws, dllm_stream_t stream) {
+  DLLM_TRY(check_shape(shape));
+  if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
+  DLLM_TRY(check_logits(logits));
+  DLLM_TRY(check_stats(out));
+  DLLM_TRY(check_ws(ws));
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kStatsOnly;
+  const dllm::StatsWs w = dllm::stats_ws_layout(ws, shape->B, shape->L, shape->V);
+  cudaError_t e = dllm::launch_stats_commit(logits, *shape, masked, *out, nullptr, ca, w,
+                                            sm_count(), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_decode_stats");
+  return ok();
+}
+
+dllm_status dllm_commit_threshold(const void* logits, const dllm_shape* shape,
+                                  const dllm_stats* stats, const dllm_block_state* state,
+                                  float tau, int32_t eos_id, void* ws, dllm_stream_t stream) {
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kThreshold;
+  ca.tau = tau;
+  ca.eos_id = eos_id;
+  return commit_common(logits, shape, stats, state, ca, ws, stream, "dllm_commit_threshold");
+}
+
+dllm_status dllm_commit_hierarchical(const void* logits, const dllm_shape* shape,
+                                     const dllm_stats* stats, const dllm_block_state* state,
+                                     float tau_low, int32_t min_width, int32_t eos_id, void* ws,
+                                     dllm_stream_t stream) {
+  if (min_width < 1) return fail(DLLM_ERR_INVALID_ARG, "min_width must be >= 1");
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kHierarchical;
+  ca.tau_low = tau_low;
+  ca.min_width = min_width;
+  ca.eos_id = eos_id;
+  return commit_common(logits, shape, stats, state, ca, ws, stream, "dllm_commit_hierarchical");
+}
+
+dllm_status dllm_commit_credit(const void* logits, const dllm_shape* shape,
+                               const dllm_stats* stats, const dllm_block_state* state,
+                               int32_t* cand_id, float* cand_credit, int32_t K, float decay,
+                               float boost, float tau, int32_t eos_id, void* ws,
+                               dllm_stream_t stream) {
+  if (!cand_id || !cand_credit)
+    return fail(DLLM_ERR_INVALID_ARG, "cand_id and cand_credit must not be null");
+  if (K < 1 || K > dllm::kMaxK)
+    return fail(K < 1 ? DLLM_ERR_INVALID_ARG : DLLM_ERR_UNSUPPORTED, "K=%d outside [1, %d]", K,
+                dllm::kMaxK);
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kCredit;
+  ca.tau = tau;
+  ca.eos_id = eos_id;
+  ca.cand_id = cand_id;
+  ca.cand_credit = cand_credit;
+  ca.K = K;
+  ca.decay = decay;
+  ca.boost = boost;
+  return commit_common(logits, shape, stats, state, ca, ws, stream, "dllm_commit_credit");
+}
+
+size_t dllm_embedding_t_elems(int32_t V, int32_t d) {
+  if (V < 1 || d < 1) return 0;
+  return static_cast<size_t>(d) * dllm::align_up(static_cast<size_t>(V), 8);
+}
+
+dllm_status dllm_prepare_embedding(const uint16_t* E, int32_t V, int32_t d, uint16_t* Et,
+                                   dllm_stream_t stream) {
+  if (!E || !Et) return fail(DLLM_ERR_INVALID_ARG, "E and Et must not be null");
+  if (V < 1 || d < 1) return fail(DLLM_ERR_INVALID_ARG, "V and d must be positive");
+  if (d % 16 != 0) return fail(DLLM_ERR_UNSUPPORTED, "d=%d is not a multiple of 16", d);
+  if (!aligned(Et, 16)) return fail(DLLM_ERR_INVALID_ARG, "Et must be 16-byte aligned");
+  const int ldt = static_cast<int>(dllm::align_up(static_cast<size_t>(V), 8));
+  cudaError_t e = dllm::launch_transpose_embedding(E, V, d, Et, ldt,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_prepare_embedding");
+  return ok();
+}
+
+size_t dllm_smooth_workspace_bytes(const dllm_shape* shape, int32_t d) {
+  if (check_shape(shape) != DLLM_OK || d < 16 || d % 16 != 0) return 0;
+  return dllm::smooth_plan(shape->B, shape->L, shape->V, d, sm_count()).ws_bytes;
+}
+
+namespace {
+
+dllm_status smooth_check(const dllm_shape* shape, int32_t d, void* ws, size_t ws_bytes,
+                         dllm::SmoothPlan* pl) {
+  DLLM_TRY(check_shape(shape));
+  DLLM_TRY(check_ws(ws));
+  if (d < 16 || d % 16 != 0 || d > 65536)
+    return fail(DLLM_ERR_UNSUPPORTED, "d=%d must be a multiple of 16 in [16, 65536]", d);
+  if (shape->V % 8 != 0)
+    return fail(DLLM_ERR_UNSUPPORTED, "smoothing needs V a multiple of 8 (V=%d)", shape->V);
+  *pl = dllm::smooth_plan(shape->B, shape->L, shape->V, d, sm_count());
+  if (ws_bytes < pl->ws_bytes)
+    return fail(DLLM_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                ws_bytes, pl->ws_bytes);
+  return DLLM_OK;
+}
+
+}  // namespace
+
+dllm_status dllm_smooth_plan_info(const dllm_shape* shape, int32_t d, int32_t* info) {
+  DLLM_TRY(check_shape(shape));
+  if (!info) return fail(DLLM_ERR_INVALID_ARG, "info is null");
+  if (d < 16 || d % 16 != 0 || d > 65536)
+    return fail(DLLM_ERR_UNSUPPORTED, "d=%d must be a multiple of 16 in [16, 65536]", d);
+  const dllm::SmoothPlan pl = dllm::smooth_plan(shape->B, shape->L, shape->V, d, sm_count());
+  info[0] = pl.m_tiles;
+  info[1] = pl.n_tiles;
+  info[2] = pl.bn_max;
+  info[3] = pl.split_k;
+  info[4] = pl.stages;
+  info[5] = 3 + (pl.split_k > 1 ? 1 : 0);  // rows, probabilities, GEMM (+ split-K reduction)
+  return ok();
+}
+
+dllm_status dllm_smooth_probs(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
+                              const dllm_block_state* state, int32_t d, int32_t* row_ids,
+                              int32_t* M, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  dllm::SmoothPlan pl;
+  DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
+  if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
+  DLLM_TRY(check_logits(logits));
+  DLLM_TRY(check_stats(stats));
+  DLLM_TRY(check_state(state));
+  if (!row_ids || !M) return fail(DLLM_ERR_INVALID_ARG, "row_ids and M must not be null");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint16_t* P = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + pl.off_p);
+  cudaError_t e = dllm::launch_compact_rows(*state, shape->B, shape->L, row_ids, M, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_smooth_probs (rows)");
+  e = dllm::launch_prob_rows(logits, *shape, stats->lse, row_ids, M, P, pl.ldp, sm_count(), st);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_smooth_probs (probabilities)");
+  return ok();
+}
+
+dllm_status dllm_smooth_gemm(const dllm_shape* shape, const uint16_t* Et, int32_t d, float* out,
+                             const int32_t* M, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  dllm::SmoothPlan pl;
+  DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
+  if (!Et || !out || !M) return fail(DLLM_ERR_INVALID_ARG, "Et, out and M must not be null");
+  if (!aligned(Et, 16) || !aligned(out, 16))
+    return fail(DLLM_ERR_INVALID_ARG, "Et and out must be 16-byte aligned");
+  const uint16_t* P =
+      reinterpret_cast<const uint16_t*>(static_cast<const char*>(ws) + pl.off_p);
+  const char* why = "launch failed";
+  const int ldt = static_cast<int>(dllm::align_up(static_cast<size_t>(shape->V), 8));
+  cudaError_t e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, M, ws,
+                                           reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess)
+    return fail(DLLM_ERR_CUDA, "dllm_smooth_gemm: %s: %s", why, cudaGetErrorString(e));
+  return ok();
+}
+
+dllm_status dllm_smooth_embed(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
+                              const dllm_block_state* state, const uint16_t* Et, int32_t d,
+                              float* out, int32_t* row_ids, int32_t* M, void* ws,
+                              size_t ws_bytes, dllm_stream_t stream) {
+  if (!Et || !out) return fail(DLLM_ERR_INVALID_ARG, "Et and out must not be null");
+  if (!aligned(Et, 16) || !aligned(out, 16))
+    return fail(DLLM_ERR_INVALID_ARG, "Et and out must be 16-byte aligned");
+  DLLM_TRY(dllm_smooth_probs(logits, shape, stats, state, d, row_ids, M, ws, ws_bytes, stream));
+  return dllm_smooth_gemm(shape, Et, d, out, M, ws, ws_bytes, stream);
+}
+
+dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32_t L,
+                                 int32_t prefix_len, int32_t window, uint8_t* refresh,
+                                 int32_t* idx, int32_t* count, dllm_stream_t stream) {
+  if (!state || !state->committed_now)
+    return fail(DLLM_ERR_INVALID_ARG, "state.committed_now is null");
+  if (!refresh || !idx || !count)
+    return fail(DLLM_ERR_INVALID_ARG, "refresh, idx and count must not be null");
+  if (B < 1 || L < 1 || prefix_len < 0 || window < 0)
+    return fail(DLLM_ERR_INVALID_ARG, "need B, L >= 1 and prefix_len, window >= 0");
+  if (static_cast<int64_t>(prefix_len) + L > 65536)
+    return fail(DLLM_ERR_UNSUPPORTED, "prefix_len + L exceeds 65536");
+  if (L > dllm::kMaxL) return fail(DLLM_ERR_UNSUPPORTED, "L=%d exceeds %d", L, dllm::kMaxL);
+  cudaError_t e = dllm::launch_kv_refresh(*state, B, L, prefix_len, window, refresh, idx, count,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_kv_refresh_mask");
+  return ok();
+}
+
+dllm_status dllm_get_status(void* ws, dllm_stream_t stream, int32_t* out_host) {
+  DLLM_TRY(check_ws(ws));
+  if (!out_host) return fail(DLLM_ERR_INVALID_ARG, "out_host is null");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_get_status");
+  *out_host = v;
+  if (v != DLLM_OK) {
+    e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "dllm_get_status (reset)");
+  }
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Host-side launch interfaces between the C ABI (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dllm.h"
+
+namespace dllm {
+
+constexpr int kMaxL = 1024;
+constexpr int kMaxK = 16;
+constexpr int kMinChunk = 2048;   // smallest vocabulary slice one CTA streams
+constexpr int kMaxSplits = 64;    // most slices per row
+
+enum CommitMode { kStatsOnly = 0, kThreshold = 1, kHierarchical = 2, kCredit = 3 };
+
+struct CommitArgs {
+  int mode;
+  float tau;
+  float tau_low;
+  int min_width;
+  int eos_id;
+  int32_t* cand_id;
+  float* cand_credit;
+  int K;
+  float decay;
+  float boost;
+};
+
+// Stats/commit workspace layout.
+struct StatsWs {
+  int32_t* status;
+  int32_t* counters;  // [B]
+  float* part_m;      // [R * S_max]
+  float* part_s;
+  int32_t* part_i;
+};
+
+int max_splits(int V);
+size_t stats_ws_bytes(int B, int L, int V);
+StatsWs stats_ws_layout(void* ws, int B, int L, int V);
+
+// Fused pass: streaming statistics (+ commit epilogue in the last CTA of each sequence).
+// masked may be null only in kStatsOnly mode (every row computed).
+cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const uint8_t* masked,
+                                const dllm_stats& stats, const dllm_block_state* state,
+                                const CommitArgs& ca, const StatsWs& ws, int sm_count,
+                                cudaStream_t stream);
+
+// Commit only, from statistics already in memory (one CTA per sequence).
+cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,
+                               const dllm_block_state& state, const CommitArgs& ca,
+                               cudaStream_t stream);
+
+// Rows kept for smoothing (masked after the commit, sequence running), compacted ascending.
+cudaError_t launch_compact_rows(const dllm_block_state& state, int B, int L, int32_t* row_ids,
+                                int32_t* M, cudaStream_t stream);
+
+cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int prefix_len,
+                              int window, uint8_t* refresh, int32_t* idx, int32_t* count,
+                              cudaStream_t stream);
+
+// Smoothing: workspace, probability rows and the tcgen05 GEMM.
+struct SmoothPlan {
+  int R;          // rows (upper bound of M)
+  int V;
+  int ldp;        // row stride of P in elements (multiple of 64)
+  int d;
+  int m_tiles;    // 128-row tiles
+  int n_tiles;    // column tiles
+  int bn_max;     // widest column tile (multiple of 16, <= 256)
+  int split_k;    // >1: partial sums reduced by a second kernel
+  int stages;     // TMA/MMA pipeline depth
+  size_t ws_bytes;
+  size_t off_p;       // bf16 P [R, ldp]
+  size_t off_part;    // fp32 partials [split_k, R_pad, d]
+};
+
+SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count);
+
+cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const float* lse,
+                             const int32_t* row_ids, const int32_t* M, uint16_t* P, int ldp,
+                             int sm_count, cudaStream_t stream);
+
+cudaError_t launch_smooth_gemm(const SmoothPlan& plan, const uint16_t* P, const uint16_t* Et,
+                               int ldt, float* out, const int32_t* M, void* ws,
+                               cudaStream_t stream, const char** why);
+
+cudaError_t launch_transpose_embedding(const uint16_t* E, int V, int d, uint16_t* Et, int ldt,
+                                       cudaStream_t stream);
+
+}  // namespace dllm

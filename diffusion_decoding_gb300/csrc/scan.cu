@@ -1,0 +1,124 @@
+// Warp-scan kernels (kernel "c"): compaction of the rows kept for iteration smoothing, and the
+// neighbourhood KV-refresh mask with its ascending index list.
+//
+// Both are tiny (at most B*L flags, or P + L cache positions per sequence) and latency-bound; they
+// use warp ballots and shuffle prefix sums, never a global barrier.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kRefreshThreads = 256;
+
+// Exclusive prefix count of `flag` over the CTA (threads in order); returns this thread's
+// offset and writes the CTA total to *total.  Ends synchronised.
+template <int NT>
+__device__ int block_exclusive_count(int flag, int* total) {
+  __shared__ int warp_cnt[NT / 32];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned bal = __ballot_sync(kFull, flag);
+  const int in_warp = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) warp_cnt[warp] = __popc(bal);
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < NT / 32 ? warp_cnt[lane] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane < NT / 32) warp_cnt[lane] = incl - v;  // exclusive
+    if (lane == 31) s_total = incl;
+  }
+  __syncthreads();
+  const int off = warp_cnt[warp] + in_warp;
+  *total = s_total;
+  __syncthreads();
+  return off;
+}
+
+__global__ void __launch_bounds__(kScanThreads) compact_rows_kernel(const uint8_t* masked,
+                                                                    const int32_t* eos_hit,
+                                                                    int B, int L, int32_t* row_ids,
+                                                                    int32_t* M) {
+  const int R = B * L;
+  int base = 0;
+  for (int r0 = 0; r0 < R; r0 += kScanThreads) {
+    const int r = r0 + threadIdx.x;
+    const int keep = (r < R) && masked[r] && !eos_hit[r / L];
+    int total;
+    const int off = block_exclusive_count<kScanThreads>(keep, &total);
+    if (keep) row_ids[base + off] = r;
+    base += total;
+  }
+  for (int k = base + threadIdx.x; k < R; k += kScanThreads) row_ids[k] = -1;
+  if (threadIdx.x == 0) *M = base;
+}
+
+// One CTA per sequence.  cnt[x] = number of block positions < x committed in this step; cache
+// position j is refreshed iff a committed block position lies in [j-P-w, j-P+w].
+__global__ void __launch_bounds__(kRefreshThreads) kv_refresh_kernel(const uint8_t* committed_now,
+                                                                     int L, int P, int w,
+                                                                     uint8_t* refresh,
+                                                                     int32_t* idx,
+                                                                     int32_t* count) {
+  extern __shared__ int cnt[];  // [L + 1]
+  const int b = blockIdx.x;
+  const int T = P + L;
+  const uint8_t* com = committed_now + static_cast<int64_t>(b) * L;
+  // inclusive prefix count of committed positions, chunk by chunk
+  if (threadIdx.x == 0) cnt[0] = 0;
+  int base = 0;
+  for (int i0 = 0; i0 < L; i0 += kRefreshThreads) {
+    const int i = i0 + threadIdx.x;
+    const int f = (i < L) && com[i];
+    int total;
+    const int off = block_exclusive_count<kRefreshThreads>(f, &total);
+    if (i < L) cnt[i + 1] = base + off + f;
+    base += total;
+  }
+  __syncthreads();
+  uint8_t* ref = refresh + static_cast<int64_t>(b) * T;
+  int32_t* ix = idx + static_cast<int64_t>(b) * T;
+  int out = 0;
+  for (int j0 = 0; j0 < T; j0 += kRefreshThreads) {
+    const int j = j0 + threadIdx.x;
+    int hit = 0;
+    if (j < T) {
+      const int lo = max(0, j - P - w);
+      const int hi = min(L - 1, j - P + w);
+      hit = (lo <= hi) && (cnt[hi + 1] - cnt[lo] > 0);
+      ref[j] = static_cast<uint8_t>(hit);
+    }
+    int total;
+    const int off = block_exclusive_count<kRefreshThreads>(hit, &total);
+    if (hit) ix[out + off] = j;
+    out += total;
+  }
+  for (int k = out + threadIdx.x; k < T; k += kRefreshThreads) ix[k] = -1;
+  if (threadIdx.x == 0) count[b] = out;
+}
+
+}  // namespace
+
+cudaError_t launch_compact_rows(const dllm_block_state& state, int B, int L, int32_t* row_ids,
+                                int32_t* M, cudaStream_t stream) {
+  compact_rows_kernel<<<1, kScanThreads, 0, stream>>>(state.masked, state.eos_hit, B, L, row_ids,
+                                                      M);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int prefix_len,
+                              int window, uint8_t* refresh, int32_t* idx, int32_t* count,
+                              cudaStream_t stream) {
+  const size_t smem = sizeof(int) * (static_cast<size_t>(L) + 1);
+  kv_refresh_kernel<<<B, kRefreshThreads, smem, stream>>>(state.committed_now, L, prefix_len,
+                                                          window, refresh, idx, count);
+  return cudaGetLastError();
+}
+
+}  // namespace dllm

@@ -1,0 +1,545 @@
+// Iteration smoothing (kernel "b"; dInfer explainer, diffusion-iteration manager): the rows left
+// undecided after this step's commit feed the next round with their whole distribution,
+//   S[j, :] = sum_v bf16(exp(z_{r_j, v} - lse_{r_j})) * E[v, :].
+//
+// Two launches: prob_rows_kernel writes the bf16 probability rows P [M, V] (compacted), then
+// smooth_gemm_kernel contracts P with the embedding table on the 5th-generation tensor cores:
+// TMA brings 128x64 tiles of P and BNx64 tiles of E^T (K-major, 128-byte swizzle) into a
+// multi-stage shared-memory ring; one thread issues tcgen05.mma (bf16 in, fp32 accumulate in
+// TMEM); four epilogue warps read the accumulator back with tcgen05.ld.  Column tiles have
+// widths that are multiples of 16 chosen so that (row tiles x column tiles) matches the SM count.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows 128 B apart,
+// 8-row groups 1024 B apart (the layout a 128-byte-swizzled TMA box of 64 bf16 columns writes).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: dense, D fp32, A and B bf16, both K-major, M x N.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+// Bounded wait on an mbarrier phase.  On timeout: raise the CTA's abort flag and record
+// DLLM_ERR_TIMEOUT in the workspace status word; every other waiter then gives up too.
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                         int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_status(status, DLLM_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Short bounded wait used only while draining after an abort.
+__device__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < 100000000ull) {
+  }
+}
+
+// ------------------------------------------------------------------ GEMM
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kUmmaK = 16;
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kATileBytes = kBM * kBK * 2;
+
+struct GemmParams {
+  int num_kb;         // 64-wide K blocks over V
+  int n_tiles;
+  int bn_base;        // narrow tile width; the first bn_rem tiles are 16 wider
+  int bn_rem;
+  int bn_max;
+  int split_k;
+  int kb_per_split;
+  int stages;
+  int tmem_cols;
+  int d;
+  int R_pad;
+  float* out;          // [M, d] when split_k == 1
+  float* part;         // [split_k, R_pad, d] otherwise
+  const int32_t* M;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    smooth_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  extern __shared__ uint8_t dyn_raw[];
+  __shared__ uint64_t bars[2 * 16 + 1];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int k_consumed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x;
+  const int ks = unit % p.split_k;
+  const int tile = unit / p.split_k;
+  const int n_tile = tile % p.n_tiles;
+  const int m_tile = tile / p.n_tiles;
+  const int m0 = m_tile * kBM;
+  const int Mdev = *reinterpret_cast<const volatile int32_t*>(p.M);
+  if (m0 >= Mdev) return;  // no rows of this tile are kept this step
+
+  const int n0 = n_tile * p.bn_base + min(n_tile, p.bn_rem) * 16;
+  const int bn = p.bn_base + (n_tile < p.bn_rem ? 16 : 0);
+  const int kb0 = ks * p.kb_per_split;
+  const int nkb = max(0, min(p.num_kb, kb0 + p.kb_per_split) - kb0);
+  const int S = p.stages;
+  const uint32_t b_tile_bytes = static_cast<uint32_t>(p.bn_max) * kBK * 2;
+
+  const uint32_t raw = smem_u32(dyn_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  const uint32_t sA = sbase;
+  const uint32_t sB = sbase + S * kATileBytes;
+  const uint32_t full0 = smem_u32(&bars[0]);
+  const uint32_t empty0 = smem_u32(&bars[16]);
+  const uint32_t acc_bar = smem_u32(&bars[32]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(acc_bar, 1);
+    abort_flag = 0;
+    k_consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_v = &abort_flag;
+  int issued = 0;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    for (int k = 0; k < nkb; ++k) {
+      const int s = k % S;
+      const uint32_t ph = (k / S) & 1;
+      if (!wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status)) break;
+      mbar_expect_tx(full0 + 8 * s, kATileBytes + b_tile_bytes);
+      tma_load_2d(sA + s * kATileBytes, &tmA, full0 + 8 * s, (kb0 + k) * kBK, m0);
+      tma_load_2d(sB + s * b_tile_bytes, &tmB, full0 + 8 * s, (kb0 + k) * kBK, n0);
+      issued = k + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    const uint32_t idesc = idesc_bf16(kBM, bn);
+    int k = 0;
+    for (; k < nkb; ++k) {
+      const int s = k % S;
+      const uint32_t ph = (k / S) & 1;
+      if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
+      tc_fence_after();
+      const uint32_t a_s = sA + s * kATileBytes;
+      const uint32_t b_s = sB + s * b_tile_bytes;
+#pragma unroll
+      for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+        umma_bf16(tmem, sw128_desc(a_s + kk * kUmmaK * 2), sw128_desc(b_s + kk * kUmmaK * 2),
+                  idesc, (k > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(empty0 + 8 * s);  // stage s is free once these MMAs have read it
+    }
+    k_consumed = k;
+    umma_commit(acc_bar);  // accumulator complete
+  } else if (warp >= 2) {
+    // ---- epilogue: TMEM -> registers -> global
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int row = m0 + q * 32 + lane;
+    // warp-uniform: tcgen05.ld below is a .sync.aligned warp instruction
+    const bool ok = __all_sync(kFull, wait_bar(acc_bar, 0, abort_v, p.status));
+    tc_fence_after();
+    if (ok) {
+      float* dst_base = p.split_k == 1
+                            ? p.out
+                            : p.part + static_cast<size_t>(ks) * p.R_pad * p.d;
+      for (int c = 0; c < bn; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+        if (row < Mdev) {
+          float4* dst = reinterpret_cast<float4*>(dst_base + static_cast<size_t>(row) * p.d + n0 + c);
+          if (nkb == 0) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_v) {
+    // drain: copies already issued and MMAs already issued must land before smem/TMEM go away
+    if (warp == 0 && lane == 0) {
+      for (int k = k_consumed; k < issued; ++k) drain_bar(full0 + 8 * (k % S), (k / S) & 1);
+    }
+    if (warp == 1 && lane == 0) drain_bar(acc_bar, 0);
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+__global__ void splitk_reduce_kernel(const float* part, int split_k, int R_pad, int d,
+                                     const int32_t* M, float* out) {
+  const int Mdev = *M;
+  const size_t n4 = static_cast<size_t>(Mdev) * d / 4;
+  const size_t slice = static_cast<size_t>(R_pad) * d / 4;
+  const float4* p4 = reinterpret_cast<const float4*>(part);
+  float4* o4 = reinterpret_cast<float4*>(out);
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float4 acc = p4[i];
+    for (int k = 1; k < split_k; ++k) {  // fixed order: deterministic
+      const float4 v = p4[k * slice + i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    o4[i] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ probability rows
+
+constexpr int kProbThreads = 256;
+
+// P[j, v] = bf16_rn(exp(z_{r_j, v} - lse_{r_j})) for j < M; 8 elements per thread-step.
+template <int DT>
+__global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* logits,
+                                                                 int64_t row_stride_bytes, int V,
+                                                                 int S, int chunk,
+                                                                 const float* lse,
+                                                                 const int32_t* row_ids,
+                                                                 const int32_t* M, uint16_t* P,
+                                                                 int ldp) {
+  const int j = blockIdx.x / S;
+  const int split = blockIdx.x - j * S;
+  if (j >= *M) return;
+  const int r = row_ids[j];
+  const float mb = lse[r] * kLog2e;
+  const char* row = logits + static_cast<int64_t>(r) * row_stride_bytes;
+  uint16_t* prow = P + static_cast<int64_t>(j) * ldp;
+  const int e0 = split * chunk;
+  const int e1 = min(V, e0 + chunk);
+  const int ngroups = (e1 - e0) / 8;
+  for (int g = threadIdx.x; g < ngroups; g += kProbThreads) {
+    const int e = e0 + g * 8;
+    float x[8];
+    if constexpr (DT == DLLM_BF16) {
+      const uint4 q = ld_stream_v4(row + static_cast<int64_t>(e) * 2);
+      x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+      x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+    } else {
+      const uint4 q0 = ld_stream_v4(row + static_cast<int64_t>(e) * 4);
+      const uint4 q1 = ld_stream_v4(row + static_cast<int64_t>(e) * 4 + 16);
+      x[0] = __uint_as_float(q0.x); x[1] = __uint_as_float(q0.y);
+      x[2] = __uint_as_float(q0.z); x[3] = __uint_as_float(q0.w);
+      x[4] = __uint_as_float(q1.x); x[5] = __uint_as_float(q1.y);
+      x[6] = __uint_as_float(q1.z); x[7] = __uint_as_float(q1.w);
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float lo = ex2(fmaf(x[2 * h], kLog2e, -mb));
+      const float hi = ex2(fmaf(x[2 * h + 1], kLog2e, -mb));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[h]) : "f"(hi), "f"(lo));
+    }
+    *reinterpret_cast<uint4*>(prow + e) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// ------------------------------------------------------------------ embedding relayout
+
+constexpr int kTT = 32;
+
+__global__ void transpose_bf16_kernel(const uint16_t* E, int V, int d, uint16_t* Et, int ldt) {
+  __shared__ uint16_t tile[kTT][kTT + 2];
+  const int v0 = blockIdx.x * kTT, c0 = blockIdx.y * kTT;
+  for (int y = threadIdx.y; y < kTT; y += blockDim.y) {
+    const int v = v0 + y, c = c0 + threadIdx.x;
+    tile[y][threadIdx.x] = (v < V && c < d) ? E[static_cast<int64_t>(v) * d + c] : uint16_t(0);
+  }
+  __syncthreads();
+  for (int y = threadIdx.y; y < kTT; y += blockDim.y) {
+    const int c = c0 + y, v = v0 + threadIdx.x;
+    if (c < d && v < ldt) Et[static_cast<int64_t>(c) * ldt + v] = tile[threadIdx.x][y];
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map: `outer` rows of `inner` elements, rows `row_bytes` apart; 128-byte
+// swizzled boxes of box_inner (= 64) x box_outer.  Out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kMaxDynSmem = 227 * 1024;
+
+}  // namespace
+
+SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
+  SmoothPlan pl{};
+  pl.R = B * L;
+  pl.V = V;
+  pl.d = d;
+  pl.ldp = static_cast<int>(align_up(V, 64));
+  pl.m_tiles = (pl.R + kBM - 1) / kBM;
+  const int units16 = d / 16;
+  const int n_min = (d + 255) / 256;
+  int n_tiles = std::max(1, sm_count / pl.m_tiles);
+  n_tiles = std::max(n_min, std::min(units16, n_tiles));
+  pl.n_tiles = n_tiles;
+  const int base = units16 / n_tiles, rem = units16 % n_tiles;
+  pl.bn_max = (base + (rem ? 1 : 0)) * 16;
+  const int num_kb = (V + kBK - 1) / kBK;
+  const int ctas = pl.m_tiles * pl.n_tiles;
+  pl.split_k = 1;
+  if (ctas * 2 <= sm_count) pl.split_k = std::max(1, std::min({8, sm_count / ctas, num_kb}));
+  const size_t stage_bytes = kATileBytes + static_cast<size_t>(pl.bn_max) * kBK * 2;
+  pl.stages = static_cast<int>(std::min<size_t>(8, (kMaxDynSmem - 2048) / stage_bytes));
+  const int R_pad = pl.m_tiles * kBM;
+  size_t off = kWsHeader;
+  off = align_up(off, 1024);
+  pl.off_p = off;
+  off += static_cast<size_t>(R_pad) * pl.ldp * 2;
+  off = align_up(off, 1024);
+  pl.off_part = off;
+  if (pl.split_k > 1) off += static_cast<size_t>(pl.split_k) * R_pad * d * 4;
+  pl.ws_bytes = align_up(off, 256);
+  return pl;
+}
+
+cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const float* lse,
+                             const int32_t* row_ids, const int32_t* M, uint16_t* P, int ldp,
+                             int sm_count, cudaStream_t stream) {
+  const int R = sh.B * sh.L;
+  const int es = sh.dtype == DLLM_BF16 ? 2 : 4;
+  // ~32 KB of logits per CTA, at least ~8 CTAs per SM
+  int S = std::max(1, sh.V / (32768 / es));
+  while (static_cast<int64_t>(R) * S < static_cast<int64_t>(sm_count) * 8 && sh.V / (S * 2) >= 2048)
+    S *= 2;
+  int chunk = static_cast<int>(align_up((sh.V + S - 1) / S, 8));
+  S = (sh.V + chunk - 1) / chunk;
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(R) * S));
+  const int64_t rsb = sh.row_stride * es;
+  if (sh.dtype == DLLM_BF16)
+    prob_rows_kernel<DLLM_BF16><<<grid, kProbThreads, 0, stream>>>(
+        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, ldp);
+  else
+    prob_rows_kernel<DLLM_F32><<<grid, kProbThreads, 0, stream>>>(
+        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, ldp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const uint16_t* Et,
+                               int ldt, float* out, const int32_t* M, void* ws,
+                               cudaStream_t stream, const char** why) {
+  const int R_pad = pl.m_tiles * kBM;
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, P, pl.V, R_pad, static_cast<uint64_t>(pl.ldp) * 2, kBK, kBM) ||
+      !make_map(&tmB, Et, pl.V, pl.d, static_cast<uint64_t>(ldt) * 2, kBK, pl.bn_max)) {
+    *why = "cuTensorMapEncodeTiled failed or is unavailable";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams gp{};
+  gp.num_kb = (pl.V + kBK - 1) / kBK;
+  gp.n_tiles = pl.n_tiles;
+  const int units16 = pl.d / 16;
+  gp.bn_base = (units16 / pl.n_tiles) * 16;
+  gp.bn_rem = units16 % pl.n_tiles;
+  gp.bn_max = pl.bn_max;
+  gp.split_k = pl.split_k;
+  gp.kb_per_split = (gp.num_kb + pl.split_k - 1) / pl.split_k;
+  gp.stages = pl.stages;
+  int cols = 32;
+  while (cols < pl.bn_max) cols *= 2;
+  gp.tmem_cols = cols;
+  gp.d = pl.d;
+  gp.R_pad = R_pad;
+  gp.out = out;
+  gp.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_part);
+  gp.M = M;
+  gp.status = static_cast<int32_t*>(ws);
+  const size_t smem = static_cast<size_t>(pl.stages) *
+                          (kATileBytes + static_cast<size_t>(pl.bn_max) * kBK * 2) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(smooth_gemm_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(pl.m_tiles * pl.n_tiles * pl.split_k));
+  smooth_gemm_kernel<<<grid, kGemmThreads, smem, stream>>>(tmA, tmB, gp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || pl.split_k == 1) return e;
+  splitk_reduce_kernel<<<std::min(1024, std::max(1, pl.R * pl.d / 4 / 256)), 256, 0, stream>>>(
+      gp.part, pl.split_k, R_pad, pl.d, M, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_embedding(const uint16_t* E, int V, int d, uint16_t* Et, int ldt,
+                                       cudaStream_t stream) {
+  const dim3 grid((ldt + kTT - 1) / kTT, (d + kTT - 1) / kTT);
+  transpose_bf16_kernel<<<grid, dim3(kTT, 8), 0, stream>>>(E, V, d, Et, ldt);
+  return cudaGetLastError();
+}
+
+}  // namespace dllm

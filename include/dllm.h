@@ -1,0 +1,242 @@
+/*
+ * dllm.h — C ABI of the parallel-decode step of a diffusion language model, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * One decode iteration of a masked-diffusion LM ends with the model's logits for a block of L
+ * positions in each of B sequences.  The step turns them into decisions: which still-masked
+ * positions to fix ("commit") now and with which token, what to feed back for the positions
+ * left open, and which KV-cache entries must be recomputed.  Sources, cited by page and
+ * section:
+ *   [dInfer explainer]  the 91haoming.cn summary of the dInfer paper (arXiv 2510.08666): its
+ *                       decoding-strategy component (threshold, hierarchical and credit
+ *                       decoding), diffusion-iteration manager (iteration smoothing), KV-cache
+ *                       manager (neighbourhood refresh) and engineering notes (early stop).
+ *   [dInfer news]       the aibase.com article: the four modules (model access, KV-cache
+ *                       manager, diffusion-iteration manager, decoding strategies).
+ * The pages give no formulas; the exact definitions these functions compute are restated at
+ * each declaration.
+ *
+ * Conventions shared by every function:
+ *  - Every pointer argument is DEVICE memory owned by the caller, except the `const dllm_*`
+ *    descriptor structs themselves and `out_host` of dllm_get_status, which are host memory
+ *    read (or written) before the function returns.  The library never allocates or frees
+ *    device memory and never synchronises the stream, except dllm_get_status.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and runs
+ *    asynchronously.  The functions hold no host state between calls, so a sequence of calls
+ *    can be captured into a CUDA graph.
+ *  - Return value: DLLM_OK when the work was enqueued.  DLLM_ERR_INVALID_ARG (a null pointer,
+ *    a non-positive size, a misaligned pointer, a stride shorter than a row) and
+ *    DLLM_ERR_UNSUPPORTED (a size beyond a documented limit) are returned before anything is
+ *    launched.  DLLM_ERR_CUDA means a launch failed.  dllm_last_error() then describes the
+ *    failure (thread-local, valid until the next call on the same thread).
+ *  - Faults found while the kernels run (a wait that timed out inside the smoothing GEMM) are
+ *    recorded in the status word at the start of the workspace; dllm_get_status reads it.
+ *  - Workspace: `ws` points to at least dllm_workspace_bytes(shape) bytes (or
+ *    dllm_smooth_workspace_bytes for dllm_smooth_embed), 256-byte aligned, zero-filled ONCE
+ *    before its first use.  The kernels leave their counters at zero when they finish, so the
+ *    same workspace serves any number of later calls on one stream.  Calls that run at the
+ *    same time must use different workspaces.
+ *
+ * Data layout (row r = b*L + i is position i of sequence b):
+ *  - logits: B*L rows of V elements, row r starting at element r*row_stride.  The pointer is
+ *    16-byte aligned; row_stride >= V.  fp32 or bf16 (dllm_shape.dtype).
+ *  - block state (dllm_block_state), all [B, L] or [B] row-major:
+ *      masked[B*L]        uint8, 1 = position still undecided;
+ *      tokens[B*L]        int32, committed token id, -1 while masked;
+ *      committed_now[B*L] uint8, written by every commit call: 1 = committed in this call;
+ *      n_commit[B]        int32, written by every commit call: number committed in this call;
+ *      eos_hit[B]         int32, set to 1 when a committed token equals eos_id; a sequence
+ *                         with eos_hit set, or with nothing masked, is stopped: later calls do
+ *                         not read its logits, commit nothing and leave its state untouched.
+ *  - statistics (dllm_stats), [B*L] each: row_max (fp32), lse (fp32, natural log-sum-exp),
+ *    conf (fp32, top-1 probability) and argmax (int32, lowest index of the maximum).  Rows not
+ *    computed hold -inf, -inf, 0 and -1.
+ */
+#ifndef DLLM_H_
+#define DLLM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* dllm_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  DLLM_OK = 0,
+  DLLM_ERR_INVALID_ARG = 1,
+  DLLM_ERR_UNSUPPORTED = 2,
+  DLLM_ERR_CUDA = 3,
+  DLLM_ERR_TIMEOUT = 4
+} dllm_status;
+
+typedef enum { DLLM_F32 = 0, DLLM_BF16 = 1 } dllm_dtype;
+
+/* Shape of one block of logits.  Limits: B >= 1, 1 <= L <= 1024, 2 <= V < 2^31,
+ * B*L <= 2^20, row_stride >= V, row_stride * element size a multiple of 16 bytes. */
+typedef struct {
+  int32_t B;
+  int32_t L;
+  int32_t V;
+  int32_t dtype;      /* dllm_dtype */
+  int64_t row_stride; /* elements between the starts of consecutive rows */
+} dllm_shape;
+
+typedef struct {
+  uint8_t* masked;
+  int32_t* tokens;
+  uint8_t* committed_now;
+  int32_t* n_commit;
+  int32_t* eos_hit;
+} dllm_block_state;
+
+typedef struct {
+  float* row_max;
+  float* lse;
+  float* conf;
+  int32_t* argmax;
+} dllm_stats;
+
+/* Description of the last error on this thread ("" if none). */
+const char* dllm_last_error(void);
+
+/* Bytes of workspace the stats and commit calls need for `shape` (0 if shape is invalid). */
+size_t dllm_workspace_bytes(const dllm_shape* shape);
+
+/*
+ * Softmax statistics of every row (dInfer explainer, decoding strategies: each strategy ranks
+ * the undecided positions by the model's confidence in its top token).  For a computed row z:
+ *   row_max = max_v z_v;  s = sum_v exp(z_v - row_max);  lse = row_max + ln s;
+ *   conf = 1/s (the top-1 probability);  argmax = lowest v with z_v = row_max.
+ * masked: [B*L] uint8 or NULL.  With a mask, only rows with masked[r] = 1 are read and
+ * computed; with NULL every row is.  Each logit crosses HBM once.
+ */
+dllm_status dllm_decode_stats(const void* logits, const dllm_shape* shape, const uint8_t* masked,
+                              const dllm_stats* out, void* ws, dllm_stream_t stream);
+
+/*
+ * Threshold decoding (dInfer explainer, decoding strategies, method 1: fix a position at once
+ * when the model is confident in it).  Per sequence that is not stopped:
+ *   C = { masked i : conf_i > tau };  if C is empty, C = { the masked i of largest conf,
+ *   lowest i on ties };  for i in C: tokens[i] = argmax_i, masked[i] = 0, committed_now[i] = 1.
+ * With logits != NULL the statistics are computed in the same pass (only the masked rows of
+ * running sequences are read) and written to *stats; with logits == NULL, *stats must hold
+ * the statistics of this step (conf and argmax are read) and the call only commits.
+ * eos_id >= 0 enables the early stop; -1 disables it.
+ */
+dllm_status dllm_commit_threshold(const void* logits, const dllm_shape* shape,
+                                  const dllm_stats* stats, const dllm_block_state* state,
+                                  float tau, int32_t eos_id, void* ws, dllm_stream_t stream);
+
+/*
+ * Hierarchical decoding (dInfer explainer, decoding strategies, method 2: split the region
+ * still to be filled recursively and decide the centre of each sub-region first).  Per
+ * sequence that is not stopped, on the mask as it stands at the call:
+ *   maximal runs [s, e) of masked positions are halved at s + floor(w/2) while their width
+ *   w >= 2*min_width; in each resulting leaf the position with conf >= tau_low that is closest
+ *   to the leaf centre (smallest |2i - (s+e-1)|, lowest i on ties) is committed; a sequence
+ *   that commits nothing commits its masked position of largest conf (lowest i on ties).
+ * min_width >= 1.  logits, stats, state and eos_id as in dllm_commit_threshold.
+ */
+dllm_status dllm_commit_hierarchical(const void* logits, const dllm_shape* shape,
+                                     const dllm_stats* stats, const dllm_block_state* state,
+                                     float tau_low, int32_t min_width, int32_t eos_id, void* ws,
+                                     dllm_stream_t stream);
+
+/*
+ * Credit decoding (dInfer explainer, decoding strategies, method 3: each candidate token of
+ * each position keeps a credit recording how often and how confidently it was chosen across
+ * iterations; stable candidates are favoured).  Per masked position of a running sequence,
+ * with top token a and confidence p:
+ *   every slot decays, c_k <- decay*c_k;  a's slot gains p (a takes the first empty slot, or
+ *   evicts the slot of least credit, lowest slot on ties, starting at p);
+ *   score = p * (1 + boost * ln(1 + c_a));
+ *   C = { i : score_i > tau }, or the masked i of largest score (lowest i) if C is empty.
+ * cand_id: [B*L, K] int32 (-1 = empty slot), cand_credit: [B*L, K] fp32, both read and
+ * updated; initialise to -1 / 0 for a fresh block.  Positions not masked keep their slots.
+ * 1 <= K <= 16.
+ */
+dllm_status dllm_commit_credit(const void* logits, const dllm_shape* shape,
+                               const dllm_stats* stats, const dllm_block_state* state,
+                               int32_t* cand_id, float* cand_credit, int32_t K, float decay,
+                               float boost, float tau, int32_t eos_id, void* ws,
+                               dllm_stream_t stream);
+
+/*
+ * Re-lay the embedding table once for the smoothing GEMM: E [V, d] bf16 row-major (the usual
+ * table) -> Et [d, ldt] bf16, Et[c, v] = E[v, c], with ldt = V rounded up to a multiple of 8
+ * (the pad columns are zeroed).  Bit patterns are copied unchanged.  d % 16 == 0.
+ */
+size_t dllm_embedding_t_elems(int32_t V, int32_t d);
+dllm_status dllm_prepare_embedding(const uint16_t* E, int32_t V, int32_t d, uint16_t* Et,
+                                   dllm_stream_t stream);
+
+/* Bytes of workspace dllm_smooth_embed needs (the bf16 probability rows and counters). */
+size_t dllm_smooth_workspace_bytes(const dllm_shape* shape, int32_t d);
+
+/*
+ * How dllm_smooth_gemm will run on the current device (host query, launches nothing):
+ * info[0] row tiles, info[1] column tiles, info[2] widest column tile, info[3] split-K factor,
+ * info[4] pipeline stages, info[5] kernels launched by one dllm_smooth_embed call.
+ */
+dllm_status dllm_smooth_plan_info(const dllm_shape* shape, int32_t d, int32_t* info);
+
+/*
+ * Iteration smoothing (dInfer explainer, diffusion-iteration manager: positions that stay
+ * undecided keep their whole distribution for the next round instead of dropping it).  After
+ * this step's commit, the rows still masked in sequences that are not stopped are listed in
+ * ascending order, row_ids[0..M), and for each
+ *   P[j, v] = bf16_round_nearest_even( exp(z_{row_ids[j], v} - lse_{row_ids[j]}) ),
+ *   out[j, :] = sum_v P[j, v] * E[v, :]       (fp32 accumulation, tensor cores)
+ * logits/shape: the step's logits (bf16 or fp32); stats: its statistics (lse is read);
+ * state: the block state after the commit (masked, eos_hit read);
+ * Et: the table from dllm_prepare_embedding; d % 16 == 0, d <= 65536;
+ * out: [B*L, d] fp32, rows >= M untouched; row_ids: [B*L] int32, entries >= M set to -1;
+ * M: one int32.  M is produced on the device; nothing is read back to the host.
+ * ws: dllm_smooth_workspace_bytes(shape, d) bytes.  V must be a multiple of 8.
+ */
+dllm_status dllm_smooth_embed(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
+                              const dllm_block_state* state, const uint16_t* Et, int32_t d,
+                              float* out, int32_t* row_ids, int32_t* M, void* ws,
+                              size_t ws_bytes, dllm_stream_t stream);
+
+/*
+ * The two halves of dllm_smooth_embed, for callers that schedule them separately (same
+ * arguments and results; call them in this order on one stream with the same workspace):
+ *   dllm_smooth_probs: rows kept (row_ids, M) and the bf16 probability rows P, written to the
+ *                      workspace;
+ *   dllm_smooth_gemm:  out[0..M) = P x E on the tensor cores.
+ */
+dllm_status dllm_smooth_probs(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
+                              const dllm_block_state* state, int32_t d, int32_t* row_ids,
+                              int32_t* M, void* ws, size_t ws_bytes, dllm_stream_t stream);
+dllm_status dllm_smooth_gemm(const dllm_shape* shape, const uint16_t* Et, int32_t d, float* out,
+                             const int32_t* M, void* ws, size_t ws_bytes, dllm_stream_t stream);
+
+/*
+ * Neighbourhood KV refresh (dInfer explainer, KV-cache manager: when a region of the sequence
+ * changes, its cache entries and those of its neighbours are recomputed).  The cache row of
+ * sequence b is [prefix 0..prefix_len) followed by the block, T = prefix_len + L entries:
+ *   refresh[b, j] = 1 iff some i with committed_now[b, i] = 1 has |j - (prefix_len + i)| <= window;
+ *   idx[b, 0..count[b]) = the refreshed j ascending, idx[b, k] = -1 for k >= count[b].
+ * refresh: [B, T] uint8; idx: [B, T] int32; count: [B] int32.  T <= 65536.
+ */
+dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32_t L,
+                                 int32_t prefix_len, int32_t window, uint8_t* refresh,
+                                 int32_t* idx, int32_t* count, dllm_stream_t stream);
+
+/*
+ * Read the device status word of a workspace (its first 4 bytes; synchronises `stream`).
+ * *out_host receives DLLM_OK or the first fault a kernel recorded there (DLLM_ERR_TIMEOUT);
+ * the word is then reset to DLLM_OK.  Works for both kinds of workspace.
+ */
+dllm_status dllm_get_status(void* ws, dllm_stream_t stream, int32_t* out_host);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLLM_H_ */

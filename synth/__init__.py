@@ -97,7 +97,7 @@ def _peak_heights(w: Workload, seed: int, it: int, attempt: int, B: int, L: int,
     return g.uniform(w.peak_lo, w.peak_hi, size=(B, L))
 
 
-def planted_ids(w: Workload, seed: int, it: int, attempt: int = 0) -> np.ndarray:
+def planted_ids(w: Workload, seed: int, it: int = 0, attempt: int = 0) -> np.ndarray:
     """Token id planted at each position in iteration ``it`` ([B, L], -1 = no plant)."""
     B, L, V = w.B, w.L, w.V
     if w.plant == "none":
@@ -130,6 +130,9 @@ def logits_f32(w: Workload, seed: int, it: int = 0, attempt: int = 0,
     """The fp32 draw std*N(0,1) + planted peaks, shape [B, L, V] (before any bf16 rounding)."""
     B, L, V = w.B, w.L, w.V
     x = normal_f32(seed, stream_id(it, attempt, _NOISE), B * L * V, 0.0, w.std).reshape(B, L, V)
+    if calibrated and w.plant == "none":
+        # the calibrated variant of an unplanted workload plants one fixed id per position
+        w = w.scaled(plant="fixed", eos_id=-1)
     ids = planted_ids(w, seed, it, attempt)
     if w.plant == "sparse":
         heights = np.full((B, L), w.peak_lo, np.float64)

@@ -1,0 +1,107 @@
+"""Shared test machinery: seeded inputs with the decision-margin guard, GPU/oracle runners.
+
+The guard keeps every decision at least 1e-3 away from its threshold (absolute) and from a tie
+(relative), so that fp32 on the GPU and double in the oracle decide alike: confidences (or
+boosted scores) vs tau, the top-2 gap of a fallback, and the least-credit gap of an eviction.  A draw that violates it
+is redrawn with the next attempt number.  Only the oracle is consulted.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+MARGIN = 1e-3
+RTOL = 2e-3
+
+
+def _gap_ok(values: np.ndarray) -> bool:
+    """Largest value ahead of the runner-up by MARGIN relative (the fallback pick)."""
+    if values.size < 2:
+        return True
+    top2 = np.sort(values)[-2:]
+    return top2[1] - top2[0] >= MARGIN * top2[1]
+
+
+def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray) -> bool:
+    """Check the guard for one step of workload w from oracle state st (not mutated)."""
+    B, L = st.B, st.L
+    conf = conf.reshape(B, L)
+    argmax = argmax.reshape(B, L)
+    scores = None
+    if w.strategy == "credit":
+        trial = st.copy()
+        scores = oracle.commit_credit(trial, conf, argmax, float(np.float32(w.decay)),
+                                      float(np.float32(w.boost)), float(np.float32(w.tau)))
+    for b in range(B):
+        m = (st.masked[b] == 1) & (st.eos_hit[b] == 0)
+        if not m.any():
+            continue
+        c = conf[b][m]
+        if w.strategy in ("threshold", "smooth"):
+            if np.any(np.abs(c - float(np.float32(w.tau))) < MARGIN):
+                return False
+            if not np.any(c > w.tau) and not _gap_ok(c):
+                return False
+        elif w.strategy == "hierarchical":
+            if np.any(np.abs(c - float(np.float32(w.tau_low))) < MARGIN):
+                return False
+            if not _gap_ok(c):  # the fallback may be taken; keep its pick unambiguous
+                return False
+        elif w.strategy == "credit":
+            s = scores[b][m]
+            if np.any(np.abs(s - float(np.float32(w.tau))) < MARGIN):
+                return False
+            if not np.any(s > w.tau) and not _gap_ok(s):
+                return False
+            for i in np.nonzero(m)[0]:
+                ids = st.cand_id[b, i]
+                if argmax[b, i] in ids or (ids == -1).any():
+                    continue
+                cr = np.sort(st.cand_credit[b, i])
+                if cr[1] - cr[0] < MARGIN * max(cr[1], 1e-30):
+                    return False
+    return True
+
+
+def oracle_step(w, st: oracle.BlockState, lg: np.ndarray, s=None):
+    """One oracle step in place (s: this step's stats if already computed)."""
+    if s is None:
+        s = oracle.stats(lg, oracle.active_rows(st.masked, st.eos_hit))
+    conf = s.conf.reshape(st.B, st.L)
+    am = s.argmax.reshape(st.B, st.L)
+    scores = None
+    if w.strategy in ("threshold", "smooth"):
+        oracle.commit_threshold(st, conf, am, float(np.float32(w.tau)), w.eos_id)
+    elif w.strategy == "hierarchical":
+        oracle.commit_hierarchical(st, conf, am, float(np.float32(w.tau_low)), w.min_width,
+                                   w.eos_id)
+    else:
+        scores = oracle.commit_credit(st, conf, am, float(np.float32(w.decay)),
+                                      float(np.float32(w.boost)), float(np.float32(w.tau)),
+                                      w.eos_id)
+    return s, scores
+
+
+def guarded_logits(w, seed: int, it: int, st: oracle.BlockState, calibrated: bool = False,
+                   max_attempts: int = 50):
+    """Logits for step `it` that satisfy the margin guard from oracle state st."""
+    for attempt in range(max_attempts):
+        lg = synth.logits(w, seed, it, attempt, calibrated)
+        act = oracle.active_rows(st.masked, st.eos_hit)
+        s = oracle.stats(lg, act)
+        if margins_ok(w, st, s.conf, s.argmax):
+            return lg, attempt, s
+    raise RuntimeError(f"no draw satisfied the margin guard after {max_attempts} attempts")
+
+
+def close(gpu: np.ndarray, ref: np.ndarray, rtol: float = RTOL) -> bool:
+    """Relative agreement, with -inf matching -inf."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    inf = np.isinf(ref)
+    if not np.array_equal(np.isinf(gpu), inf) or not np.array_equal(gpu[inf], ref[inf]):
+        return False
+    g, r = gpu[~inf], ref[~inf]
+    return bool(np.all(np.abs(g - r) <= rtol * np.abs(r) + 1e-30))

@@ -1,0 +1,219 @@
+"""GPU vs oracle: statistics and the three commit strategies, element by element.
+
+Small cases span several vocabulary slices with ragged tails; the full cases are the five
+workloads at their stated sizes, in the launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_runner import GpuDecoder, to_device
+from harness import close, guarded_logits, oracle_step
+
+import diffusion_decoding_gb300 as dd
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare_step(gpu: GpuDecoder, ost: oracle.BlockState, os_, scores=None, tag=""):
+    hs = gpu.host_state()
+    for k in ("masked", "tokens", "committed_now", "n_commit", "eos_hit"):
+        assert np.array_equal(hs[k], getattr(ost, k)), f"{tag}: {k} differs"
+    st = gpu.host_stats()
+    assert np.array_equal(st["argmax"], os_.argmax), f"{tag}: argmax differs"
+    assert close(st["row_max"], os_.row_max, 0.0), f"{tag}: row_max differs"
+    assert close(st["lse"], os_.lse), f"{tag}: lse differs"
+    assert close(st["conf"], os_.conf), f"{tag}: conf differs"
+    if gpu.w.strategy == "credit":
+        assert np.array_equal(hs["cand_id"], ost.cand_id), f"{tag}: candidate ids differ"
+        assert close(hs["cand_credit"], ost.cand_credit), f"{tag}: credits differ"
+
+
+def _run_loop(w, seed, calibrated=False, max_iters=None):
+    gpu = GpuDecoder(w)
+    ost = oracle.BlockState(w.B, w.L, w.K)
+    iters = w.max_iters if max_iters is None else max_iters
+    n_done = 0
+    for it in range(iters):
+        running = ((ost.masked.sum(1) > 0) & (ost.eos_hit == 0)).any()
+        if not running:
+            break
+        lg, _, s = guarded_logits(w, seed, it, ost, calibrated)
+        s_ref, scores = oracle_step(w, ost, lg, s)
+        gpu.step(to_device(lg))
+        torch.cuda.synchronize()
+        _compare_step(gpu, ost, s_ref, scores, tag=f"{w.key} iter {it}")
+        n_done += 1
+    return gpu, ost, n_done
+
+
+# ------------------------------------------------------------------ statistics
+
+@pytest.mark.parametrize("V", [1, 7, 8, 9, 100, 2049, 5003, 33001, 126464])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_stats_ragged_sizes(V, dtype):
+    w = synth.WORKLOADS["threshold_loop"].scaled(B=3, L=5, V=V, dtype=dtype)
+    lg = synth.logits(w, seed=V, it=1)
+    rng = np.random.default_rng(V)
+    masked = (rng.random(w.B * w.L) < 0.7).astype(np.uint8)
+    ref = oracle.stats(lg, masked)
+    stats = dd.StatsBuffers(w.B * w.L)
+    shape = dd.make_shape(w.B, w.L, V, dd.DLLM_BF16 if dtype == "bf16" else dd.DLLM_F32)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape))
+    dd.dllm_decode_stats(to_device(lg), shape, torch.from_numpy(masked).cuda(), stats, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(stats.argmax.cpu().numpy(), ref.argmax)
+    assert close(stats.row_max.cpu().numpy(), ref.row_max, 0.0)
+    assert close(stats.lse.cpu().numpy(), ref.lse)
+    assert close(stats.conf.cpu().numpy(), ref.conf)
+    # no mask: every row computed
+    dd.dllm_decode_stats(to_device(lg), shape, None, stats, ws)
+    full = oracle.stats(lg)
+    assert np.array_equal(stats.argmax.cpu().numpy(), full.argmax)
+    assert close(stats.conf.cpu().numpy(), full.conf)
+
+
+def test_stats_padded_row_stride_and_ties():
+    B, L, V, pad = 2, 3, 4000, 64
+    rng = np.random.default_rng(1)
+    base = rng.integers(-3, 4, size=(B * L, V)).astype(np.float32)  # many exact ties
+    buf = np.zeros((B * L, V + pad), np.float32)
+    buf[:, :V] = base
+    buf[:, V:] = 1e4  # padding must never be read
+    t = torch.from_numpy(buf).cuda()
+    shape = dd.make_shape(B, L, V, dd.DLLM_F32, row_stride=V + pad)
+    stats = dd.StatsBuffers(B * L)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape))
+    dd.dllm_decode_stats(t, shape, None, stats, ws)
+    ref = oracle.stats(base)
+    assert np.array_equal(stats.argmax.cpu().numpy(), ref.argmax)
+    assert close(stats.lse.cpu().numpy(), ref.lse)
+
+
+def test_stats_deterministic():
+    w = synth.WORKLOADS["credit_loop"].scaled(B=4, L=8)
+    lg = to_device(synth.logits(w, seed=3))
+    shape = dd.make_shape(w.B, w.L, w.V, dd.DLLM_BF16)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape))
+    a, b = dd.StatsBuffers(w.B * w.L), dd.StatsBuffers(w.B * w.L)
+    dd.dllm_decode_stats(lg, shape, None, a, ws)
+    dd.dllm_decode_stats(lg, shape, None, b, ws)
+    for k in ("row_max", "lse", "conf", "argmax"):
+        assert torch.equal(getattr(a, k), getattr(b, k))
+
+
+# ------------------------------------------------------------------ the five workloads
+
+def test_threshold_single_step_full():
+    w = synth.WORKLOADS["threshold_single"]
+    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key])
+    assert n == 1 and ost.n_commit[0] >= 1
+
+
+def test_threshold_loop_full():
+    w = synth.WORKLOADS["threshold_loop"]
+    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key])
+    assert n >= 1
+
+
+@pytest.mark.parametrize("seed", [5, 6])
+def test_threshold_loop_calibrated_small(seed):
+    w = synth.WORKLOADS["threshold_loop"].scaled(B=4, L=32, V=20000)
+    gpu, ost, n = _run_loop(w, seed, calibrated=True)
+    assert n >= 2
+
+
+def test_hierarchical_loop_full():
+    w = synth.WORKLOADS["hierarchical_loop"]
+    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key])
+    assert ost.masked.sum() == 0
+
+
+@pytest.mark.parametrize("L,min_width", [(64, 2), (100, 3), (33, 1)])
+def test_hierarchical_calibrated_small(L, min_width):
+    w = synth.WORKLOADS["hierarchical_loop"].scaled(B=5, L=L, V=8200, min_width=min_width,
+                                                     max_iters=L)
+    gpu, ost, n = _run_loop(w, 40 + L, calibrated=True)
+    assert ost.masked.sum() == 0
+
+
+def test_credit_loop_full():
+    w = synth.WORKLOADS["credit_loop"]
+    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key])
+    assert n == w.max_iters
+
+
+@pytest.mark.parametrize("K", [8, 3])
+def test_credit_calibrated_small(K):
+    w = synth.WORKLOADS["credit_loop"].scaled(B=6, L=24, V=12000, K=K, max_iters=20)
+    gpu, ost, n = _run_loop(w, 70 + K, calibrated=True)
+    assert n >= 5
+
+
+def test_large_block_epilogue():
+    # L = 1024 positions: the epilogue loops 4 positions per thread, scans cross 8 warps
+    w = synth.WORKLOADS["hierarchical_loop"].scaled(B=2, L=1024, V=2048, max_iters=3)
+    _run_loop(w, 90, calibrated=True)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_stopped_sequences_are_untouched():
+    w = synth.WORKLOADS["threshold_loop"].scaled(B=3, L=8, V=512, eos_id=-1)
+    gpu = GpuDecoder(w)
+    gpu.state.masked.view(3, 8)[0].zero_()        # nothing masked
+    gpu.state.eos_hit[1] = 1                      # EOS already hit
+    before = gpu.host_state()
+    lg = to_device(synth.logits(w, seed=2))
+    gpu.step(lg)
+    after = gpu.host_state()
+    assert after["n_commit"].tolist()[:2] == [0, 0] and after["n_commit"][2] >= 1
+    assert np.array_equal(after["masked"][:2], before["masked"][:2])
+    st = gpu.host_stats()
+    assert (st["argmax"].reshape(3, 8)[:2] == -1).all()
+    assert np.isneginf(st["lse"].reshape(3, 8)[:2]).all()
+
+
+def test_commit_only_matches_fused():
+    w = synth.WORKLOADS["credit_loop"].scaled(B=4, L=16, V=3000, max_iters=6)
+    fused, split = GpuDecoder(w), GpuDecoder(w)
+    for it in range(w.max_iters):
+        lg = to_device(synth.logits(w, seed=11, it=it, calibrated=True))
+        fused.step(lg)
+        dd.dllm_decode_stats(lg, split.shape, split.state.masked, split.stats, split.ws)
+        # rows of stopped sequences are skipped by the fused call; none stop here
+        split.step(None)
+        a, b = fused.host_state(), split.host_state()
+        for k in a:
+            assert np.array_equal(a[k], b[k]), k
+
+
+def test_graph_capture_replays_steps():
+    w = synth.WORKLOADS["threshold_loop"].scaled(B=2, L=16, V=4096, max_iters=4)
+    lgs = [to_device(synth.logits(w, seed=8, it=i, calibrated=True)) for i in range(4)]
+    eager = GpuDecoder(w)
+    for lg in lgs:
+        eager.step(lg)
+    graphed = GpuDecoder(w)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for lg in lgs:
+                graphed.step(lg)
+    graphed.state.reset()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = eager.host_state(), graphed.host_state()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_status_word_stays_ok():
+    w = synth.WORKLOADS["threshold_single"]
+    gpu = GpuDecoder(w)
+    gpu.step(to_device(synth.logits(w, seed=1)))
+    assert dd.dllm_get_status(gpu.ws) == dd.DLLM_OK

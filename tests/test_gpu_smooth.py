@@ -1,0 +1,138 @@
+"""GPU vs oracle: iteration smoothing (probability rows + tcgen05 GEMM) and the KV refresh."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_runner import GpuDecoder, to_device
+from harness import guarded_logits, oracle_step
+
+import diffusion_decoding_gb300 as dd
+
+pytestmark = pytest.mark.gpu
+
+
+def smooth_close(g: np.ndarray, o: np.ndarray, rtol=2e-3) -> None:
+    """Per element |g-o| <= rtol*max(|o|, 1e-2*max_row|o|); per row relative L2 <= rtol."""
+    g = np.asarray(g, np.float64)
+    floor = 1e-2 * np.abs(o).max(axis=1, keepdims=True)
+    bound = rtol * np.maximum(np.abs(o), floor)
+    bad = np.abs(g - o) > bound
+    assert not bad.any(), f"{bad.sum()} elements outside the bound; worst " \
+                          f"{np.max(np.abs(g - o) / np.maximum(bound, 1e-30)):.3g}x"
+    rel = np.linalg.norm(g - o, axis=1) / np.maximum(np.linalg.norm(o, axis=1), 1e-30)
+    assert (rel <= rtol).all(), rel.max()
+
+
+def _table(V, d, seed=77):
+    E = synth.embedding_table(seed, V, d)
+    Et = torch.empty(dd.dllm_embedding_t_elems(V, d), dtype=torch.int16, device="cuda")
+    dd.dllm_prepare_embedding(torch.from_numpy(E.view(np.int16)).cuda(), Et)
+    return E, Et
+
+
+def _smooth_case(w, seed, calibrated, sample_rows=None):
+    """One full step: threshold commit, smoothing, refresh; returns GPU and oracle results."""
+    gpu = GpuDecoder(w)
+    ost = oracle.BlockState(w.B, w.L)
+    lg, _, s = guarded_logits(w, seed, 0, ost, calibrated)
+    s_ref, _ = oracle_step(w, ost, lg, s)
+    E, Et = _table(w.V, w.d)
+    R = w.B * w.L
+    out = torch.full((R, w.d), float("nan"), dtype=torch.float32, device="cuda")
+    row_ids = torch.empty(R, dtype=torch.int32, device="cuda")
+    M = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws_s = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
+    T = w.prefix_len + w.L
+    refresh = torch.empty(w.B * T, dtype=torch.uint8, device="cuda")
+    idx = torch.empty(w.B * T, dtype=torch.int32, device="cuda")
+    count = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    lgd = to_device(lg)
+    gpu.step(lgd)
+    dd.dllm_smooth_embed(lgd, gpu.shape, gpu.stats, gpu.state, Et, w.d, out, row_ids, M, ws_s)
+    dd.dllm_kv_refresh_mask(gpu.state, w.prefix_len, w.window, refresh, idx, count)
+    torch.cuda.synchronize()
+    assert dd.dllm_get_status(ws_s) == dd.DLLM_OK
+    # commits, rows, refresh: exact
+    hs = gpu.host_state()
+    for k in ("masked", "tokens", "committed_now", "n_commit"):
+        assert np.array_equal(hs[k], getattr(ost, k)), k
+    ids_ref = oracle.smooth_rows(ost.masked, ost.eos_hit)
+    Mg = int(M.item())
+    assert Mg == len(ids_ref)
+    rid = row_ids.cpu().numpy()
+    assert np.array_equal(rid[:Mg], ids_ref) and (rid[Mg:] == -1).all()
+    ref_r, ref_i, ref_c = oracle.kv_refresh(ost.committed_now, w.prefix_len, w.window)
+    assert np.array_equal(refresh.cpu().numpy().reshape(w.B, T), ref_r)
+    assert np.array_equal(idx.cpu().numpy().reshape(w.B, T), ref_i)
+    assert np.array_equal(count.cpu().numpy(), ref_c)
+    # soft embeddings: all rows or a sample, against the oracle's own lse
+    o = out.cpu().numpy()
+    assert np.isnan(o[Mg:]).all(), "rows >= M must stay untouched"
+    js = np.arange(Mg) if sample_rows is None else np.unique(
+        np.linspace(0, Mg - 1, sample_rows).astype(int))
+    ref = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids_ref[js].astype(np.int32), E)
+    smooth_close(o[js], ref)
+    return Mg
+
+
+@pytest.mark.parametrize("B,L,V,d", [
+    (1, 8, 1024, 32),        # one row tile, one column tile
+    (3, 100, 2056, 160),     # 3 row tiles with a ragged last one, V not a multiple of 64
+    (2, 64, 4096, 272),      # column tiles of unequal widths
+    (4, 64, 6000, 2048),     # full embedding width
+])
+def test_smooth_small_all_rows(B, L, V, d):
+    w = synth.WORKLOADS["smooth_step"].scaled(B=B, L=L, V=V, d=d, prefix_len=16)
+    Mg = _smooth_case(w, seed=B * 1000 + V, calibrated=True)
+    assert Mg > 0
+
+
+def test_smooth_step_full_sampled_rows():
+    w = synth.WORKLOADS["smooth_step"]
+    Mg = _smooth_case(w, synth.workloads.SEEDS[w.key], calibrated=False, sample_rows=6)
+    assert Mg == w.B * w.L - w.B  # literal workload: one fallback commit per sequence
+
+
+def test_smooth_skips_when_nothing_is_masked():
+    w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=8, V=1024, d=32)
+    gpu = GpuDecoder(w)
+    gpu.state.masked.zero_()
+    E, Et = _table(w.V, w.d)
+    out = torch.full((16, 32), 7.0, device="cuda")
+    row_ids = torch.empty(16, dtype=torch.int32, device="cuda")
+    M = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+    ws = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
+    lg = to_device(synth.logits(w, seed=1))
+    dd.dllm_decode_stats(lg, gpu.shape, None, gpu.stats, gpu.ws)
+    dd.dllm_smooth_embed(lg, gpu.shape, gpu.stats, gpu.state, Et, w.d, out, row_ids, M, ws)
+    torch.cuda.synchronize()
+    assert int(M.item()) == 0 and (row_ids.cpu() == -1).all() and (out.cpu() == 7.0).all()
+
+
+def test_embedding_relayout_is_a_transpose():
+    V, d = 1001, 48
+    E, Et = _table(V, d)
+    ldt = dd.dllm_embedding_t_elems(V, d) // d
+    et = Et.cpu().numpy().view(np.uint16).reshape(d, ldt)
+    assert np.array_equal(et[:, :V], E.T) and (et[:, V:] == 0).all()
+
+
+@pytest.mark.parametrize("B,L,P,w", [(1, 1, 0, 0), (3, 64, 1024, 4), (2, 300, 5, 9),
+                                     (4, 1024, 0, 1), (2, 16, 3, 40)])
+def test_kv_refresh_random_patterns(B, L, P, w):
+    rng = np.random.default_rng(B * L + P)
+    com = (rng.random((B, L)) < 0.1).astype(np.uint8)
+    com[0, :] = 0  # one sequence with no commit
+    state = dd.BlockState(B, L)
+    state.committed_now.copy_(torch.from_numpy(com.reshape(-1)))
+    T = P + L
+    refresh = torch.empty(B * T, dtype=torch.uint8, device="cuda")
+    idx = torch.empty(B * T, dtype=torch.int32, device="cuda")
+    count = torch.empty(B, dtype=torch.int32, device="cuda")
+    dd.dllm_kv_refresh_mask(state, P, w, refresh, idx, count)
+    r, i, c = oracle.kv_refresh(com, P, w)
+    assert np.array_equal(refresh.cpu().numpy().reshape(B, T), r)
+    assert np.array_equal(idx.cpu().numpy().reshape(B, T), i)
+    assert np.array_equal(count.cpu().numpy(), c)
