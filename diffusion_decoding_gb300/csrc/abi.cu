@@ -110,6 +110,15 @@ dllm_status commit_common(const void* logits, const dllm_shape* shape, const dll
 
 }  // namespace
 
+namespace dllm {
+void set_last_error(const char* msg, cudaError_t e) {
+  if (e != cudaSuccess)
+    snprintf(g_err, sizeof(g_err), "%s: %s", msg, cudaGetErrorString(e));
+  else
+    snprintf(g_err, sizeof(g_err), "%s", msg);
+}
+}  // namespace dllm
+
 extern "C" {
 
 const char* dllm_last_error(void) { return g_err; }
@@ -182,7 +191,7 @@ dllm_status dllm_commit_credit(const void* logits, const dllm_shape* shape,
 
 size_t dllm_embedding_t_elems(int32_t V, int32_t d) {
   if (V < 1 || d < 1) return 0;
-  return static_cast<size_t>(d) * dllm::align_up(static_cast<size_t>(V), 8);
+  return static_cast<size_t>(d) * dllm::align_up(static_cast<size_t>(V), 64);
 }
 
 dllm_status dllm_prepare_embedding(const uint16_t* E, int32_t V, int32_t d, uint16_t* Et,
@@ -191,8 +200,8 @@ dllm_status dllm_prepare_embedding(const uint16_t* E, int32_t V, int32_t d, uint
   if (V < 1 || d < 1) return fail(DLLM_ERR_INVALID_ARG, "V and d must be positive");
   if (d % 16 != 0) return fail(DLLM_ERR_UNSUPPORTED, "d=%d is not a multiple of 16", d);
   if (!aligned(Et, 16)) return fail(DLLM_ERR_INVALID_ARG, "Et must be 16-byte aligned");
-  const int ldt = static_cast<int>(dllm::align_up(static_cast<size_t>(V), 8));
-  cudaError_t e = dllm::launch_transpose_embedding(E, V, d, Et, ldt,
+  const int Vp = static_cast<int>(dllm::align_up(static_cast<size_t>(V), 64));
+  cudaError_t e = dllm::launch_transpose_embedding(E, V, d, Et, Vp,
                                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "dllm_prepare_embedding");
   return ok();
@@ -251,7 +260,8 @@ dllm_status dllm_smooth_probs(const void* logits, const dllm_shape* shape, const
   uint16_t* P = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + pl.off_p);
   cudaError_t e = dllm::launch_compact_rows(*state, shape->B, shape->L, row_ids, M, st);
   if (e != cudaSuccess) return cuda_fail(e, "dllm_smooth_probs (rows)");
-  e = dllm::launch_prob_rows(logits, *shape, stats->lse, row_ids, M, P, pl.ldp, sm_count(), st);
+  e = dllm::launch_prob_rows(logits, *shape, stats->lse, row_ids, M, P, pl.m_tiles * 128,
+                             sm_count(), st);
   if (e != cudaSuccess) return cuda_fail(e, "dllm_smooth_probs (probabilities)");
   return ok();
 }

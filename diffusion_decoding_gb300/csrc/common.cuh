@@ -24,7 +24,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 16-byte streaming load that bypasses L1 (every logit is read once).
+// 16-byte streaming load that bypasses L1 (every logit is read once per kernel).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

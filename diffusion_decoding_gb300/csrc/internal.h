@@ -11,8 +11,6 @@ namespace dllm {
 
 constexpr int kMaxL = 1024;
 constexpr int kMaxK = 16;
-constexpr int kMinChunk = 2048;   // smallest vocabulary slice one CTA streams
-constexpr int kMaxSplits = 64;    // most slices per row
 
 enum CommitMode { kStatsOnly = 0, kThreshold = 1, kHierarchical = 2, kCredit = 3 };
 
@@ -32,7 +30,6 @@ struct CommitArgs {
 // Stats/commit workspace layout.
 struct StatsWs {
   int32_t* status;
-  int32_t* counters;  // [B]
   float* part_m;      // [R * S_max]
   float* part_s;
   int32_t* part_i;
@@ -66,7 +63,7 @@ cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int p
 struct SmoothPlan {
   int R;          // rows (upper bound of M)
   int V;
-  int ldp;        // row stride of P in elements (multiple of 64)
+  int ldp;        // V rounded up to 64 (64-wide K slabs)
   int d;
   int m_tiles;    // 128-row tiles
   int n_tiles;    // column tiles
@@ -74,21 +71,24 @@ struct SmoothPlan {
   int split_k;    // >1: partial sums reduced by a second kernel
   int stages;     // TMA/MMA pipeline depth
   size_t ws_bytes;
-  size_t off_p;       // bf16 P [R, ldp]
+  size_t off_p;       // bf16 P, K-slab-blocked [ldp / 64][R_pad][64]
   size_t off_part;    // fp32 partials [split_k, R_pad, d]
 };
 
 SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count);
 
 cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const float* lse,
-                             const int32_t* row_ids, const int32_t* M, uint16_t* P, int ldp,
+                             const int32_t* row_ids, const int32_t* M, uint16_t* P, int R_pad,
                              int sm_count, cudaStream_t stream);
 
 cudaError_t launch_smooth_gemm(const SmoothPlan& plan, const uint16_t* P, const uint16_t* Et,
                                int ldt, float* out, const int32_t* M, void* ws,
                                cudaStream_t stream, const char** why);
 
-cudaError_t launch_transpose_embedding(const uint16_t* E, int V, int d, uint16_t* Et, int ldt,
+// Record a message for dllm_last_error() on this thread (with a CUDA error string if e != 0).
+void set_last_error(const char* msg, cudaError_t e);
+
+cudaError_t launch_transpose_embedding(const uint16_t* E, int V, int d, uint16_t* Et, int Vp,
                                        cudaStream_t stream);
 
 }  // namespace dllm

@@ -2,12 +2,13 @@
 // undecided after this step's commit feed the next round with their whole distribution,
 //   S[j, :] = sum_v bf16(exp(z_{r_j, v} - lse_{r_j})) * E[v, :].
 //
-// Two launches: prob_rows_kernel writes the bf16 probability rows P [M, V] (compacted), then
-// smooth_gemm_kernel contracts P with the embedding table on the 5th-generation tensor cores:
-// TMA brings 128x64 tiles of P and BNx64 tiles of E^T (K-major, 128-byte swizzle) into a
-// multi-stage shared-memory ring; one thread issues tcgen05.mma (bf16 in, fp32 accumulate in
-// TMEM); four epilogue warps read the accumulator back with tcgen05.ld.  Column tiles have
-// widths that are multiples of 16 chosen so that (row tiles x column tiles) matches the SM count.
+// Two launches: prob_rows_kernel writes the bf16 probability rows P (compacted), then
+// smooth_gemm_kernel contracts P with the embedding table on the 5th-generation tensor cores.
+// Both operands are stored K-slab-blocked, [ceil(V/64)][rows][64]: the 64-wide K slab of every
+// row is contiguous, so each 128-row TMA box is one contiguous 16 KB block (with K = V = 126464
+// a plain row-major box would touch a different memory page in every row).  TMA brings the
+// boxes (128-byte swizzle) into a multi-stage shared-memory ring; tcgen05.mma accumulates in
+// TMEM; epilogue warps read the accumulator back with tcgen05.ld.
 #include <cuda.h>
 
 #include <algorithm>
@@ -49,28 +50,67 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
+// Box (0, y, slab) of a K-slab-blocked operand: rows y.. of one 64-wide K slab.
+__device__ __forceinline__ void tma_load_slab(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                              int y, int slab) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(y), "r"(slab)
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+// Tensor-memory allocation for a CTA pair: one warp in EACH of the two CTAs executes these
+// collectively; both CTAs receive the same column base.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Arrive (release, cluster scope) on an mbarrier that may live in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -81,21 +121,26 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// Pair MMA issued by the leader CTA: D[256 x N] (+)= A[256 x 16] * B[N x 16]^T, bf16 inputs,
+// fp32 accumulators.  Each CTA holds 128 rows of A and N/2 rows of B at the same shared-memory
+// offsets, and receives its own 128 rows of D in its tensor memory.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
+// Arrive on the mbarrier at offset `bar` in both CTAs of the pair once every tcgen05 operation
+// issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  const uint16_t mask = 0x3;
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
       : "memory");
 }
 
@@ -132,12 +177,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitim
 
 // Bounded wait on an mbarrier phase.  On timeout: raise the CTA's abort flag and record
 // DLLM_ERR_TIMEOUT in the workspace status word; every other waiter then gives up too.
+template <bool kCluster = false>
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                          int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -156,16 +205,18 @@ __device__ void drain_bar(uint32_t bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ GEMM
 
-constexpr int kBM = 128;
-constexpr int kBK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kBM = 128;   // rows per CTA; a CTA pair covers 256
+constexpr int kBK = 64;    // one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;
-constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 TMEM + MMA (leader) / forwarder (peer),
+                                   // warps 2-5 epilogue
 constexpr int kATileBytes = kBM * kBK * 2;
+constexpr int kMaxStages = 8;
 
 struct GemmParams {
   int num_kb;         // 64-wide K blocks over V
   int n_tiles;
-  int bn_base;        // narrow tile width; the first bn_rem tiles are 16 wider
+  int bn_base;        // narrow pair-tile width; the first bn_rem tiles are 16 wider
   int bn_rem;
   int bn_max;
   int split_k;
@@ -180,43 +231,53 @@ struct GemmParams {
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
+// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep TMA
+// ring.  The peer CTA forwards each landed stage to the leader's "full" barrier; the leader's
+// MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each stage's
+// release, and finally the accumulator-ready signal, to both CTAs.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     smooth_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   extern __shared__ uint8_t dyn_raw[];
-  __shared__ uint64_t bars[2 * 16 + 1];
+  __shared__ uint64_t bars[2 * kMaxStages + 1];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ int k_consumed;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x;
-  const int ks = unit % p.split_k;
-  const int tile = unit / p.split_k;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int ks = pair % p.split_k;
+  const int tile = pair / p.split_k;
   const int n_tile = tile % p.n_tiles;
-  const int m_tile = tile / p.n_tiles;
-  const int m0 = m_tile * kBM;
+  const int m_pair = tile / p.n_tiles;
+  const int m0 = m_pair * 2 * kBM;
   const int Mdev = *reinterpret_cast<const volatile int32_t*>(p.M);
-  if (m0 >= Mdev) return;  // no rows of this tile are kept this step
+  if (m0 >= Mdev) return;  // both CTAs of the pair leave together: no row of the pair is kept
 
+  const int my_m0 = m0 + static_cast<int>(rank) * kBM;
   const int n0 = n_tile * p.bn_base + min(n_tile, p.bn_rem) * 16;
   const int bn = p.bn_base + (n_tile < p.bn_rem ? 16 : 0);
+  const int my_n0 = n0 + static_cast<int>(rank) * (bn / 2);
   const int kb0 = ks * p.kb_per_split;
   const int nkb = max(0, min(p.num_kb, kb0 + p.kb_per_split) - kb0);
   const int S = p.stages;
-  const uint32_t b_tile_bytes = static_cast<uint32_t>(p.bn_max) * kBK * 2;
+  const uint32_t b_half_bytes = static_cast<uint32_t>(p.bn_max / 2) * kBK * 2;
 
   const uint32_t raw = smem_u32(dyn_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + S * kATileBytes;
   const uint32_t full0 = smem_u32(&bars[0]);
-  const uint32_t empty0 = smem_u32(&bars[16]);
-  const uint32_t acc_bar = smem_u32(&bars[32]);
+  const uint32_t empty0 = smem_u32(&bars[kMaxStages]);
+  const uint32_t acc_bar = smem_u32(&bars[2 * kMaxStages]);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      // leader: its own producer's expect-tx arrival + the peer's forwarded arrival
+      mbar_init(full0 + 8 * s, leader ? 2 : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     mbar_init(acc_bar, 1);
@@ -225,51 +286,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_slot), p.tmem_cols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tmem_slot), p.tmem_cols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before anyone signals across the pair
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_v = &abort_flag;
   int issued = 0;
 
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer
+    // ---- TMA producer (both CTAs): own 128 rows of P, own half of the E^T tile
     for (int k = 0; k < nkb; ++k) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
       if (!wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status)) break;
-      mbar_expect_tx(full0 + 8 * s, kATileBytes + b_tile_bytes);
-      tma_load_2d(sA + s * kATileBytes, &tmA, full0 + 8 * s, (kb0 + k) * kBK, m0);
-      tma_load_2d(sB + s * b_tile_bytes, &tmB, full0 + 8 * s, (kb0 + k) * kBK, n0);
+      mbar_expect_tx(full0 + 8 * s, kATileBytes + b_half_bytes);
+      tma_load_slab(sA + s * kATileBytes, &tmA, full0 + 8 * s, my_m0, kb0 + k);
+      tma_load_slab(sB + s * b_half_bytes, &tmB, full0 + 8 * s, my_n0, kb0 + k);
       issued = k + 1;
     }
+  } else if (warp == 1 && lane == 0 && !leader) {
+    // ---- forwarder (peer): tell the leader when each of this CTA's stages has landed
+    const uint32_t leader_full0 = map_to_rank(full0, 0);
+    for (int k = 0; k < nkb; ++k) {
+      const int s = k % S;
+      const uint32_t ph = (k / S) & 1;
+      if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
+      mbar_arrive_remote(leader_full0 + 8 * s);
+    }
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    const uint32_t idesc = idesc_bf16(kBM, bn);
+    // ---- MMA issuer (leader)
+    const uint32_t idesc = idesc_bf16(2 * kBM, bn);
     int k = 0;
     for (; k < nkb; ++k) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
-      if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
+      if (!wait_bar<true>(full0 + 8 * s, ph, abort_v, p.status)) break;
       tc_fence_after();
       const uint32_t a_s = sA + s * kATileBytes;
-      const uint32_t b_s = sB + s * b_tile_bytes;
+      const uint32_t b_s = sB + s * b_half_bytes;
 #pragma unroll
       for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-        umma_bf16(tmem, sw128_desc(a_s + kk * kUmmaK * 2), sw128_desc(b_s + kk * kUmmaK * 2),
-                  idesc, (k > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16_pair(tmem, sw128_desc(a_s + kk * kUmmaK * 2), sw128_desc(b_s + kk * kUmmaK * 2),
+                       idesc, (k > 0 || kk > 0) ? 1u : 0u);
       }
-      umma_commit(empty0 + 8 * s);  // stage s is free once these MMAs have read it
+      umma_commit_pair(empty0 + 8 * s);  // stage s is free in both CTAs once these MMAs read it
     }
     k_consumed = k;
-    umma_commit(acc_bar);  // accumulator complete
+    umma_commit_pair(acc_bar);  // accumulators complete in both CTAs
   } else if (warp >= 2) {
-    // ---- epilogue: TMEM -> registers -> global
+    // ---- epilogue (both CTAs): this CTA's 128 accumulator rows, TMEM -> registers -> global
     const int q = warp & 3;  // TMEM lane quarter this warp may read
-    const int row = m0 + q * 32 + lane;
+    const int row = my_m0 + q * 32 + lane;
     // warp-uniform: tcgen05.ld below is a .sync.aligned warp instruction
     const bool ok = __all_sync(kFull, wait_bar(acc_bar, 0, abort_v, p.status));
     tc_fence_after();
@@ -281,7 +352,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t v[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
         if (row < Mdev) {
-          float4* dst = reinterpret_cast<float4*>(dst_base + static_cast<size_t>(row) * p.d + n0 + c);
+          float4* dst =
+              reinterpret_cast<float4*>(dst_base + static_cast<size_t>(row) * p.d + n0 + c);
           if (nkb == 0) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0u;
@@ -304,9 +376,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 1 && lane == 0) drain_bar(acc_bar, 0);
     __syncthreads();
   }
+  cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may still touch it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, p.tmem_cols);
+    tmem_dealloc_pair(tmem, p.tmem_cols);
   }
 }
 
@@ -335,7 +408,9 @@ __global__ void splitk_reduce_kernel(const float* part, int split_k, int R_pad, 
 
 constexpr int kProbThreads = 256;
 
-// P[j, v] = bf16_rn(exp(z_{r_j, v} - lse_{r_j})) for j < M; 8 elements per thread-step.
+// P[j, v] = bf16_rn(exp(z_{r_j, v} - lse_{r_j})) for j < M, 8 elements per thread-step, stored
+// K-slab-blocked: element (j, v) at ((v / 64) * R_pad + j) * 64 + v % 64.  The columns of the
+// last slab beyond V are written as zeros (the GEMM reads whole slabs).
 template <int DT>
 __global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* logits,
                                                                  int64_t row_stride_bytes, int V,
@@ -343,40 +418,44 @@ __global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* log
                                                                  const float* lse,
                                                                  const int32_t* row_ids,
                                                                  const int32_t* M, uint16_t* P,
-                                                                 int ldp) {
+                                                                 int R_pad) {
   const int j = blockIdx.x / S;
   const int split = blockIdx.x - j * S;
   if (j >= *M) return;
   const int r = row_ids[j];
   const float mb = lse[r] * kLog2e;
   const char* row = logits + static_cast<int64_t>(r) * row_stride_bytes;
-  uint16_t* prow = P + static_cast<int64_t>(j) * ldp;
   const int e0 = split * chunk;
-  const int e1 = min(V, e0 + chunk);
+  const int e1 = min(static_cast<int>(align_up(V, 64)), e0 + chunk);
   const int ngroups = (e1 - e0) / 8;
   for (int g = threadIdx.x; g < ngroups; g += kProbThreads) {
     const int e = e0 + g * 8;
-    float x[8];
-    if constexpr (DT == DLLM_BF16) {
-      const uint4 q = ld_stream_v4(row + static_cast<int64_t>(e) * 2);
-      x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
-      x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
-    } else {
-      const uint4 q0 = ld_stream_v4(row + static_cast<int64_t>(e) * 4);
-      const uint4 q1 = ld_stream_v4(row + static_cast<int64_t>(e) * 4 + 16);
-      x[0] = __uint_as_float(q0.x); x[1] = __uint_as_float(q0.y);
-      x[2] = __uint_as_float(q0.z); x[3] = __uint_as_float(q0.w);
-      x[4] = __uint_as_float(q1.x); x[5] = __uint_as_float(q1.y);
-      x[6] = __uint_as_float(q1.z); x[7] = __uint_as_float(q1.w);
-    }
-    uint32_t w[4];
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (e < V) {
+      float x[8];
+      if constexpr (DT == DLLM_BF16) {
+        const uint4 q = ld_stream_v4(row + static_cast<int64_t>(e) * 2);
+        x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+        x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+      } else {
+        const uint4 q0 = ld_stream_v4(row + static_cast<int64_t>(e) * 4);
+        const uint4 q1 = ld_stream_v4(row + static_cast<int64_t>(e) * 4 + 16);
+        x[0] = __uint_as_float(q0.x); x[1] = __uint_as_float(q0.y);
+        x[2] = __uint_as_float(q0.z); x[3] = __uint_as_float(q0.w);
+        x[4] = __uint_as_float(q1.x); x[5] = __uint_as_float(q1.y);
+        x[6] = __uint_as_float(q1.z); x[7] = __uint_as_float(q1.w);
+      }
+      uint32_t w[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float lo = ex2(fmaf(x[2 * h], kLog2e, -mb));
-      const float hi = ex2(fmaf(x[2 * h + 1], kLog2e, -mb));
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[h]) : "f"(hi), "f"(lo));
+      for (int h = 0; h < 4; ++h) {
+        const float lo = ex2(fmaf(x[2 * h], kLog2e, -mb));
+        const float hi = ex2(fmaf(x[2 * h + 1], kLog2e, -mb));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[h]) : "f"(hi), "f"(lo));
+      }
+      out = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *reinterpret_cast<uint4*>(prow + e) = make_uint4(w[0], w[1], w[2], w[3]);
+    uint16_t* dst = P + ((static_cast<int64_t>(e >> 6) * R_pad + j) << 6) + (e & 63);
+    *reinterpret_cast<uint4*>(dst) = out;
   }
 }
 
@@ -384,7 +463,8 @@ __global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* log
 
 constexpr int kTT = 32;
 
-__global__ void transpose_bf16_kernel(const uint16_t* E, int V, int d, uint16_t* Et, int ldt) {
+// Et[(v / 64) * d + c][v % 64] = E[v][c]  (K-slab-blocked transpose; zeros for v >= V).
+__global__ void transpose_bf16_kernel(const uint16_t* E, int V, int d, uint16_t* Et, int Vp) {
   __shared__ uint16_t tile[kTT][kTT + 2];
   const int v0 = blockIdx.x * kTT, c0 = blockIdx.y * kTT;
   for (int y = threadIdx.y; y < kTT; y += blockDim.y) {
@@ -394,7 +474,8 @@ __global__ void transpose_bf16_kernel(const uint16_t* E, int V, int d, uint16_t*
   __syncthreads();
   for (int y = threadIdx.y; y < kTT; y += blockDim.y) {
     const int c = c0 + y, v = v0 + threadIdx.x;
-    if (c < d && v < ldt) Et[static_cast<int64_t>(c) * ldt + v] = tile[threadIdx.x][y];
+    if (c < d && v < Vp)
+      Et[((static_cast<int64_t>(v >> 6) * d + c) << 6) + (v & 63)] = tile[threadIdx.x][y];
   }
 }
 
@@ -418,17 +499,17 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map: `outer` rows of `inner` elements, rows `row_bytes` apart; 128-byte
-// swizzled boxes of box_inner (= 64) x box_outer.  Out-of-range elements read as zero.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-              uint32_t box_inner, uint32_t box_outer) {
+// K-slab-blocked bf16 operand [slabs][rows][64] as a 3-D tensor map; boxes of 64 x box_rows x 1
+// with 128-byte swizzle (the K-major layout tcgen05 descriptors expect).
+bool make_slab_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t slabs,
+                   uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  cuuint64_t dims[3] = {64, rows, slabs};
+  cuuint64_t strides[2] = {128, rows * 128};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -442,21 +523,37 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
   pl.R = B * L;
   pl.V = V;
   pl.d = d;
-  pl.ldp = static_cast<int>(align_up(V, 64));
-  pl.m_tiles = (pl.R + kBM - 1) / kBM;
+  pl.ldp = static_cast<int>(align_up(V, 64));  // slabs x 64
+  const int m_pairs = (pl.R + 2 * kBM - 1) / (2 * kBM);
+  pl.m_tiles = 2 * m_pairs;
   const int units16 = d / 16;
-  const int n_min = (d + 255) / 256;
-  int n_tiles = std::max(1, sm_count / pl.m_tiles);
-  n_tiles = std::max(n_min, std::min(units16, n_tiles));
-  pl.n_tiles = n_tiles;
-  const int base = units16 / n_tiles, rem = units16 % n_tiles;
-  pl.bn_max = (base + (rem ? 1 : 0)) * 16;
   const int num_kb = (V + kBK - 1) / kBK;
-  const int ctas = pl.m_tiles * pl.n_tiles;
-  pl.split_k = 1;
-  if (ctas * 2 <= sm_count) pl.split_k = std::max(1, std::min({8, sm_count / ctas, num_kb}));
-  const size_t stage_bytes = kATileBytes + static_cast<size_t>(pl.bn_max) * kBK * 2;
-  pl.stages = static_cast<int>(std::min<size_t>(8, (kMaxDynSmem - 2048) / stage_bytes));
+  const int pair_slots = std::max(1, sm_count / 2);
+  // Pick (column tiles, split-K) for one wave of CTA pairs, minimising K-blocks per pair x
+  // (BN + 64): wide tiles carry more MMA work per byte staged, and each extra split costs a
+  // round trip of fp32 partial sums.  Only when one wave cannot hold the grid are more waves
+  // allowed (then each wave is charged in full).
+  double best = 1e300;
+  for (int nt = (units16 + 15) / 16; nt <= units16; ++nt) {
+    const int base = units16 / nt, rem = units16 % nt;
+    const int bn_max = (base + (rem ? 1 : 0)) * 16;
+    if (bn_max > 256) continue;
+    for (int sk = 1; sk <= std::min(8, num_kb); ++sk) {
+      const long pairs = static_cast<long>(m_pairs) * nt * sk;
+      const long waves = (pairs + pair_slots - 1) / pair_slots;
+      const double kb = static_cast<double>((num_kb + sk - 1) / sk);
+      const double est = (waves > 1 ? 4.0 * waves : 1.0) * kb * (bn_max + 64.0) +
+                         (sk > 1 ? 0.02 * num_kb * 256.0 * sk : 0.0);
+      if (est < best - 1e-9) {
+        best = est;
+        pl.n_tiles = nt;
+        pl.bn_max = bn_max;
+        pl.split_k = sk;
+      }
+    }
+  }
+  const size_t stage_bytes = kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2;
+  pl.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage_bytes));
   const int R_pad = pl.m_tiles * kBM;
   size_t off = kWsHeader;
   off = align_up(off, 1024);
@@ -470,7 +567,7 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
 }
 
 cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const float* lse,
-                             const int32_t* row_ids, const int32_t* M, uint16_t* P, int ldp,
+                             const int32_t* row_ids, const int32_t* M, uint16_t* P, int R_pad,
                              int sm_count, cudaStream_t stream) {
   const int R = sh.B * sh.L;
   const int es = sh.dtype == DLLM_BF16 ? 2 : 4;
@@ -478,16 +575,17 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
   int S = std::max(1, sh.V / (32768 / es));
   while (static_cast<int64_t>(R) * S < static_cast<int64_t>(sm_count) * 8 && sh.V / (S * 2) >= 2048)
     S *= 2;
-  int chunk = static_cast<int>(align_up((sh.V + S - 1) / S, 8));
-  S = (sh.V + chunk - 1) / chunk;
+  const int Vp = static_cast<int>(align_up(sh.V, 64));
+  int chunk = static_cast<int>(align_up((Vp + S - 1) / S, 8));
+  S = (Vp + chunk - 1) / chunk;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(R) * S));
   const int64_t rsb = sh.row_stride * es;
   if (sh.dtype == DLLM_BF16)
     prob_rows_kernel<DLLM_BF16><<<grid, kProbThreads, 0, stream>>>(
-        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, ldp);
+        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
   else
     prob_rows_kernel<DLLM_F32><<<grid, kProbThreads, 0, stream>>>(
-        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, ldp);
+        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
   return cudaGetLastError();
 }
 
@@ -496,8 +594,10 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
                                cudaStream_t stream, const char** why) {
   const int R_pad = pl.m_tiles * kBM;
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, P, pl.V, R_pad, static_cast<uint64_t>(pl.ldp) * 2, kBK, kBM) ||
-      !make_map(&tmB, Et, pl.V, pl.d, static_cast<uint64_t>(ldt) * 2, kBK, pl.bn_max)) {
+  const uint64_t slabs = static_cast<uint64_t>(pl.ldp) / 64;
+  (void)ldt;
+  if (!make_slab_map(&tmA, P, R_pad, slabs, kBM) ||
+      !make_slab_map(&tmB, Et, pl.d, slabs, pl.bn_max / 2)) {
     *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;
   }
@@ -521,11 +621,12 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.M = M;
   gp.status = static_cast<int32_t*>(ws);
   const size_t smem = static_cast<size_t>(pl.stages) *
-                          (kATileBytes + static_cast<size_t>(pl.bn_max) * kBK * 2) + 1024;
+                          (kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2) + 1024;
   cudaError_t e = cudaFuncSetAttribute(smooth_gemm_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  // m_tiles = 2 x row pairs: one CTA per 128 rows, clusters of 2 along x
   const dim3 grid(static_cast<unsigned>(pl.m_tiles * pl.n_tiles * pl.split_k));
   smooth_gemm_kernel<<<grid, kGemmThreads, smem, stream>>>(tmA, tmB, gp);
   e = cudaGetLastError();
@@ -535,10 +636,10 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_embedding(const uint16_t* E, int V, int d, uint16_t* Et, int ldt,
+cudaError_t launch_transpose_embedding(const uint16_t* E, int V, int d, uint16_t* Et, int Vp,
                                        cudaStream_t stream) {
-  const dim3 grid((ldt + kTT - 1) / kTT, (d + kTT - 1) / kTT);
-  transpose_bf16_kernel<<<grid, dim3(kTT, 8), 0, stream>>>(E, V, d, Et, ldt);
+  const dim3 grid((Vp + kTT - 1) / kTT, (d + kTT - 1) / kTT);
+  transpose_bf16_kernel<<<grid, dim3(kTT, 8), 0, stream>>>(E, V, d, Et, Vp);
   return cudaGetLastError();
 }
 

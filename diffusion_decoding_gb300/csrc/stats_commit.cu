@@ -1,12 +1,14 @@
-// Fused softmax statistics + commit decision over one masked block (kernel "a").
+// Softmax statistics + commit decision over one masked block (kernel "a": two launches).
 //
-// Every masked row of logits is streamed from HBM exactly once.  A row is cut into S vocabulary
-// slices; each CTA reduces one slice to a partial (max, rescaled sum, argmax) with 128-bit loads
-// and warp-shuffle merges, writes it to the workspace and bumps its sequence's counter.  The CTA
-// that arrives last for a sequence merges the L*S partials of that sequence into the row
-// statistics and runs the commit decision in shared memory (threshold, hierarchical or credit
-// decoding; dInfer explainer, decoding-strategy component, methods 1-3), then re-arms the
-// counter.  Nothing waits on another CTA: the last arriver is found with one atomic.
+// 1. stats_partials_kernel: every masked row of logits is streamed from HBM exactly once.  Rows
+//    are cut into 4 KB slices; each warp owns one slice, issues all of its 128-bit loads up
+//    front (8 per lane), takes the slice maximum with warp shuffles, sums exp(z - max) against
+//    that single maximum (no rescaling), finds the first index of the maximum, and writes one
+//    partial (max, sum, argmax).  Warps never wait for one another: no block barrier, no atomic.
+// 2. merge_commit_kernel (one CTA per sequence, chained with programmatic dependent launch so it
+//    is resident before the first kernel drains): merges the L x S partials of its sequence into
+//    the row statistics and runs the commit decision in shared memory (threshold, hierarchical
+//    or credit decoding; dInfer explainer, decoding-strategy component, methods 1-3).
 #include <algorithm>
 #include <climits>
 
@@ -17,8 +19,7 @@ namespace dllm {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;
+constexpr int kMaxWarps = kThreads / 32;
 
 struct CommitCtx {
   int B, L;
@@ -29,7 +30,7 @@ struct CommitCtx {
 struct FusedParams {
   const char* logits;
   int64_t row_stride_bytes;
-  int V, S, chunk, vec;
+  int V, S, chunk;
   const uint8_t* masked;   // rows to read (state.masked when committing)
   const int32_t* eos_hit;  // null in statistics-only mode
   dllm_stats stats;
@@ -42,25 +43,44 @@ struct CommitOnlyParams {
   CommitCtx c;
 };
 
-// ------------------------------------------------------------------ per-thread streaming
+// ------------------------------------------------------------------ slice reduction
 
-template <int N>
-__device__ __forceinline__ void acc_elems(RowAcc& a, const float* x, int base) {
-  float vm = x[0];
-#pragma unroll
-  for (int j = 1; j < N; ++j) vm = fmaxf(vm, x[j]);
-  if (vm > a.m) {  // new running maximum: rescale the sum once, remember the first index
-    int j0 = 0;
-#pragma unroll
-    for (int j = N - 1; j >= 0; --j)
-      if (x[j] == vm) j0 = j;
-    a.s = a.s * ex2((a.m - vm) * kLog2e);
-    a.m = vm;
-    a.idx = base + j0;
+constexpr int kVecs = 8;  // 16-byte vectors per lane: one warp slice = 4 KB
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+template <int DT>
+struct SliceTraits;
+template <>
+struct SliceTraits<DLLM_BF16> {
+  static constexpr int VEC = 8, ES = 2;
+  static constexpr uint32_t kNegInf = 0xFF80FF80u;  // two bf16 -inf
+};
+template <>
+struct SliceTraits<DLLM_F32> {
+  static constexpr int VEC = 4, ES = 4;
+  static constexpr uint32_t kNegInf = 0xFF800000u;  // fp32 -inf
+};
+
+// elements of one warp slice
+template <int DT>
+constexpr int slice_elems() {
+  return 32 * kVecs * SliceTraits<DT>::VEC;
+}
+
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& q) {
+  if constexpr (DT == DLLM_BF16) {
+    const uint32_t m = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
+    return fmaxf(bf16lo(m), bf16hi(m));
+  } else {
+    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
   }
-  const float mb = (a.m == -INFINITY) ? 0.f : a.m * kLog2e;
-#pragma unroll
-  for (int j = 0; j < N; ++j) a.s += ex2(fmaf(x[j], kLog2e, -mb));
 }
 
 template <int DT>
@@ -76,50 +96,72 @@ __device__ __forceinline__ void unpack16(const uint4& q, float* x) {
   }
 }
 
-// Reduce elements [e0, e1) of one row into this thread's accumulator.  Each thread visits its
-// elements in increasing index order, so a strict '>' keeps the lowest index of the maximum.
+// One warp reduces elements [e0, e0 + n) of a row (n <= slice_elems) to (max, sum of
+// exp(z - max), lowest index of max).  The slice maximum is taken first, then every lane sums
+// exp(z - max) against that single maximum; only lanes holding the maximum look for its index.
+// The result is valid in every lane.
 template <int DT>
-__device__ __forceinline__ void stream_slice(const char* row, int64_t e0, int64_t e1, int vec,
-                                             RowAcc& acc) {
-  constexpr int VEC = DT == DLLM_BF16 ? 8 : 4;
-  constexpr int ES = DT == DLLM_BF16 ? 2 : 4;
-  const int tid = threadIdx.x;
-  int64_t tail = e0;
-  if (vec) {
-    const int nvec = static_cast<int>((e1 - e0) / VEC);
-    const char* base = row + e0 * ES;
-    for (int v0 = 0; v0 < nvec; v0 += kThreads * kUnroll) {
-      uint4 q[kUnroll];
+__device__ __forceinline__ RowAcc warp_reduce_slice(const char* row, int64_t e0, int n) {
+  using T = SliceTraits<DT>;
+  const int lane = threadIdx.x & 31;
+  const int nvec = n * T::ES / 16;
+  const int ntail = n - nvec * T::VEC;
+  const char* base = row + e0 * T::ES;
+  uint4 q[kVecs];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int vi = v0 + u * kThreads + tid;
-        if (vi < nvec) q[u] = ld_stream_v4(base + static_cast<int64_t>(vi) * 16);
-      }
+  for (int u = 0; u < kVecs; ++u) {
+    const int vi = u * 32 + lane;
+    q[u] = vi < nvec ? ld_stream_v4(base + static_cast<int64_t>(vi) * 16)
+                     : make_uint4(T::kNegInf, T::kNegInf, T::kNegInf, T::kNegInf);
+  }
+  const float xt = lane < ntail ? load_logit(row, DT, e0 + nvec * T::VEC + lane) : -INFINITY;
+
+  float tm = xt;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int vi = v0 + u * kThreads + tid;
-        if (vi < nvec) {
-          float x[VEC];
-          unpack16<DT>(q[u], x);
-          acc_elems<VEC>(acc, x, static_cast<int>(e0) + vi * VEC);
-        }
-      }
+  for (int u = 0; u < kVecs; ++u) tm = fmaxf(tm, vec_max<DT>(q[u]));
+  float m = tm;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+
+  const float mb = (m == -INFINITY) ? 0.f : m * kLog2e;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < kVecs; ++u) {
+    float x[T::VEC];
+    unpack16<DT>(q[u], x);
+#pragma unroll
+    for (int j = 0; j < T::VEC; ++j) acc[j & 3] += ex2(fmaf(x[j], kLog2e, -mb));
+  }
+  acc[0] += ex2(fmaf(xt, kLog2e, -mb));
+  float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  int idx = INT_MAX;
+  if (tm == m && m != -INFINITY) {  // rare: this lane holds the slice maximum
+#pragma unroll
+    for (int u = kVecs - 1; u >= 0; --u) {
+      float x[T::VEC];
+      unpack16<DT>(q[u], x);
+#pragma unroll
+      for (int j = T::VEC - 1; j >= 0; --j)
+        if (x[j] == m) idx = (u * 32 + lane) * T::VEC + j;
     }
-    tail = e0 + static_cast<int64_t>(nvec) * VEC;
+    if (xt == m && idx == INT_MAX) idx = nvec * T::VEC + lane;
   }
-  for (int64_t e = tail + tid; e < e1; e += kThreads) {
-    float x[1] = {load_logit(row, DT, e)};
-    acc_elems<1>(acc, x, static_cast<int>(e));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sum += __shfl_xor_sync(kFull, sum, o);
+    idx = min(idx, __shfl_xor_sync(kFull, idx, o));
   }
+  return RowAcc{m, sum, idx == INT_MAX ? -1 : static_cast<int>(e0) + idx};
 }
 
 // ------------------------------------------------------------------ block helpers
 
 // In-place inclusive max-scan of a[0..n) (values >= -1) with warp shuffles; ends synchronised.
 __device__ void block_max_scan(int* a, int n) {
-  __shared__ int warp_tot[kWarps];
+  __shared__ int warp_tot[kMaxWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ipt = (n + kThreads - 1) / kThreads;
+  const int nt = blockDim.x;
+  const int ipt = (n + nt - 1) / nt;
   const int beg = tid * ipt, end = min(n, beg + ipt);
   int run = -1;
   for (int i = beg; i < end; ++i) {
@@ -144,13 +186,14 @@ __device__ void block_max_scan(int* a, int n) {
 
 // Masked position of largest value, lowest index on ties (-1 if nothing is masked).
 __device__ int block_masked_argmax(const float* val, const uint8_t* mask, int L) {
-  __shared__ float wv[kWarps];
-  __shared__ int wi[kWarps];
+  __shared__ float wv[kMaxWarps];
+  __shared__ int wi[kMaxWarps];
   __shared__ int result;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nt = blockDim.x, nw = nt >> 5;
   float best = -INFINITY;
   int bi = INT_MAX;
-  for (int i = tid; i < L; i += kThreads) {
+  for (int i = tid; i < L; i += nt) {
     if (mask[i] && (bi == INT_MAX || val[i] > best)) {
       best = val[i];
       bi = i;
@@ -173,7 +216,7 @@ __device__ int block_masked_argmax(const float* val, const uint8_t* mask, int L)
   if (tid == 0) {
     float b = wv[0];
     int i0 = wi[0];
-    for (int w = 1; w < kWarps; ++w) {
+    for (int w = 1; w < nw; ++w) {
       if (wi[w] != INT_MAX && (i0 == INT_MAX || wv[w] > b || (wv[w] == b && wi[w] < i0))) {
         b = wv[w];
         i0 = wi[w];
@@ -227,20 +270,21 @@ __device__ __forceinline__ void leaf_of(const EpiSmem& sm, int L, int min_width,
 __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const EpiSmem& sm) {
   __shared__ int s_count;
   const int tid = threadIdx.x;
+  const int nt = blockDim.x;
   const int L = c.L;
   const dllm_block_state& st = c.state;
   const int64_t r0 = static_cast<int64_t>(b) * L;
   if (stopped) {
-    for (int i = tid; i < L; i += kThreads) st.committed_now[r0 + i] = 0;
+    for (int i = tid; i < L; i += nt) st.committed_now[r0 + i] = 0;
     if (tid == 0) st.n_commit[b] = 0;
     return;
   }
   const int mode = c.ca.mode;
   if (mode == kThreshold) {
-    for (int i = tid; i < L; i += kThreads) sm.sel[i] = (sm.mask[i] && sm.val[i] > c.ca.tau) ? 1 : 0;
+    for (int i = tid; i < L; i += nt) sm.sel[i] = (sm.mask[i] && sm.val[i] > c.ca.tau) ? 1 : 0;
   } else if (mode == kCredit) {
     const int K = c.ca.K;
-    for (int i = tid; i < L; i += kThreads) {
+    for (int i = tid; i < L; i += nt) {
       sm.sel[i] = 0;
       if (!sm.mask[i]) continue;
       int32_t* ids = c.ca.cand_id + (r0 + i) * K;
@@ -277,7 +321,7 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
       sm.sel[i] = score > c.ca.tau ? 1 : 0;
     }
   } else {  // hierarchical
-    for (int i = tid; i < L; i += kThreads) {
+    for (int i = tid; i < L; i += nt) {
       sm.scan1[i] = sm.mask[i] ? -1 : i;
       sm.scan2[i] = sm.mask[L - 1 - i] ? -1 : i;
       sm.key[i] = INT_MAX;
@@ -286,14 +330,14 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
     block_max_scan(sm.scan1, L);
     block_max_scan(sm.scan2, L);
     const int mw = c.ca.min_width;
-    for (int i = tid; i < L; i += kThreads) {
+    for (int i = tid; i < L; i += nt) {
       if (!sm.mask[i] || !(sm.val[i] >= c.ca.tau_low)) continue;
       int s, e;
       leaf_of(sm, L, mw, i, &s, &e);
       atomicMin(&sm.key[s], abs(2 * i - (s + e - 1)) * 2048 + i);
     }
     __syncthreads();
-    for (int i = tid; i < L; i += kThreads) {
+    for (int i = tid; i < L; i += nt) {
       sm.sel[i] = 0;
       if (!sm.mask[i] || !(sm.val[i] >= c.ca.tau_low)) continue;
       int s, e;
@@ -303,7 +347,7 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
   }
   __syncthreads();
   int any = 0;
-  for (int i = tid; i < L; i += kThreads) any |= sm.sel[i];
+  for (int i = tid; i < L; i += nt) any |= sm.sel[i];
   any = __syncthreads_or(any);
   if (!any) {  // at least one commit per step: the best-ranked masked position
     const int best = block_masked_argmax(sm.val, sm.mask, L);
@@ -313,7 +357,7 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
   if (tid == 0) s_count = 0;
   __syncthreads();
   int cnt = 0, eos = 0;
-  for (int i = tid; i < L; i += kThreads) {
+  for (int i = tid; i < L; i += nt) {
     const uint8_t sel = sm.sel[i];
     st.committed_now[r0 + i] = sel;
     if (sel) {
@@ -334,94 +378,101 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
 
 // ------------------------------------------------------------------ kernels
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads) stats_commit_kernel(FusedParams p) {
-  extern __shared__ __align__(16) uint8_t dyn[];
-  __shared__ RowAcc warp_acc[kWarps];
-  __shared__ int s_last;
+// Last CTA of sequence b: merge the L*S slice partials into row statistics, then decide the
+// commits.  Kept out of line so that its registers do not constrain the streaming loop.
+__device__ __noinline__ void sequence_epilogue(const FusedParams& p, int b, uint8_t* dyn) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nt = blockDim.x, nw = nt >> 5;
   const int L = p.c.L;
-  const int r = blockIdx.x / p.S;
-  const int split = blockIdx.x - r * p.S;
-  const int b = r / L;
-
-  const bool active = (p.masked == nullptr || p.masked[r]) &&
-                      !(p.eos_hit != nullptr && p.eos_hit[b]);
-  RowAcc acc = row_acc_empty();
-  if (active) {
-    const int64_t e0 = static_cast<int64_t>(split) * p.chunk;
-    const int64_t e1 = min(static_cast<int64_t>(p.V), e0 + p.chunk);
-    stream_slice<DT>(p.logits + static_cast<int64_t>(r) * p.row_stride_bytes, e0, e1, p.vec,
-                     acc);
-  }
-  acc = row_acc_warp_reduce(acc);
-  if (lane == 0) warp_acc[warp] = acc;
-  __syncthreads();
-  if (warp == 0) {
-    RowAcc a = lane < kWarps ? warp_acc[lane] : row_acc_empty();
-    a = row_acc_warp_reduce(a);
-    if (lane == 0) {
-      const int64_t pi = static_cast<int64_t>(r) * p.S + split;
-      p.ws.part_m[pi] = a.m;
-      p.ws.part_s[pi] = a.s;
-      p.ws.part_i[pi] = a.idx;
-      __threadfence();
-      const int prev = atomicAdd(&p.ws.counters[b], 1);
-      s_last = (prev == L * p.S - 1);
-    }
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // ---- last CTA of sequence b: merge the partials, then decide the commits
   const EpiSmem sm = carve(dyn, L);
   const bool committing = p.c.ca.mode != kStatsOnly;
   int any_masked = 0;
-  for (int i = tid; i < L; i += kThreads) {
+  for (int i = tid; i < L; i += nt) {
     const uint8_t m = p.masked ? p.masked[static_cast<int64_t>(b) * L + i] : 1;
     sm.mask[i] = m;
     any_masked |= m;
   }
   any_masked = __syncthreads_or(any_masked);
   const bool stopped = committing && ((p.eos_hit && p.eos_hit[b]) || !any_masked);
+  // merge: each warp takes rows warp, warp+nw, ...; the partial loads of up to kRowBatch rows
+  // are issued together so the L2 round trips overlap
+  constexpr int kRowBatch = 8;
   const int S = p.S;
-  for (int i = warp; i < L; i += kWarps) {
-    const int64_t row = static_cast<int64_t>(b) * L + i;
-    const bool act = sm.mask[i] && !stopped;
-    RowAcc a = row_acc_empty();
-    if (act) {
+  for (int i0 = warp; i0 < L; i0 += nw * kRowBatch) {
+    RowAcc a[kRowBatch];
+#pragma unroll
+    for (int k = 0; k < kRowBatch; ++k) {
+      a[k] = row_acc_empty();
+      const int i = i0 + k * nw;
+      if (i >= L || !sm.mask[i] || stopped) continue;
+      const int64_t row = static_cast<int64_t>(b) * L + i;
       for (int j = lane; j < S; j += 32) {
         const int64_t pi = row * S + j;
         RowAcc q{__ldcg(p.ws.part_m + pi), __ldcg(p.ws.part_s + pi), __ldcg(p.ws.part_i + pi)};
-        a = row_acc_merge(a, q);
+        a[k] = row_acc_merge(a[k], q);
       }
     }
-    a = row_acc_warp_reduce(a);
-    if (lane == 0) {
-      float rm = -INFINITY, l = -INFINITY, cf = 0.f;
-      int am = -1;
-      if (act) {
-        rm = a.m;
-        l = a.m + logf(a.s);
-        cf = 1.f / a.s;
-        am = a.idx;
+#pragma unroll
+    for (int k = 0; k < kRowBatch; ++k) {
+      const int i = i0 + k * nw;
+      const RowAcc t = row_acc_warp_reduce(a[k]);
+      if (lane == 0 && i < L) {
+        const int64_t row = static_cast<int64_t>(b) * L + i;
+        const bool act = sm.mask[i] && !stopped;
+        float rm = -INFINITY, l = -INFINITY, cf = 0.f;
+        int am = -1;
+        if (act) {
+          rm = t.m;
+          l = t.m + logf(t.s);
+          cf = 1.f / t.s;
+          am = t.idx;
+        }
+        p.stats.row_max[row] = rm;
+        p.stats.lse[row] = l;
+        p.stats.conf[row] = cf;
+        p.stats.argmax[row] = am;
+        sm.val[i] = cf;
+        sm.am[i] = am;
       }
-      p.stats.row_max[row] = rm;
-      p.stats.lse[row] = l;
-      p.stats.conf[row] = cf;
-      p.stats.argmax[row] = am;
-      sm.val[i] = cf;
-      sm.am[i] = am;
     }
   }
   __syncthreads();
   if (committing) commit_sequence(p.c, b, stopped, sm);
-  if (tid == 0) p.ws.counters[b] = 0;  // re-arm for the next launch on this workspace
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams p) {
+  // let the merge kernel's CTAs become resident while this grid drains
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp;
+  const int S = p.S, L = p.c.L;
+  const int64_t n_items = static_cast<int64_t>(p.c.B) * L * S;
+  if (item >= n_items) return;
+  const int64_t r = item / S;
+  const int sl = static_cast<int>(item - r * S);
+  const bool active = (p.masked == nullptr || p.masked[r]) &&
+                      !(p.eos_hit != nullptr && p.eos_hit[r / L]);
+  if (!active) return;  // the merge kernel never reads partials of rows that are not read
+  const int64_t e0 = static_cast<int64_t>(sl) * p.chunk;
+  const int n = static_cast<int>(min(static_cast<int64_t>(p.V), e0 + p.chunk) - e0);
+  const RowAcc a = warp_reduce_slice<DT>(p.logits + r * p.row_stride_bytes, e0, n);
+  if (lane == 0) {
+    p.ws.part_m[item] = a.m;
+    p.ws.part_s[item] = a.s;
+    p.ws.part_i[item] = a.idx;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) merge_commit_kernel(FusedParams p) {
+  extern __shared__ __align__(1024) uint8_t dyn[];
+  // every partial, and every read of the block state, of the first kernel is complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  sequence_epilogue(p, blockIdx.x, dyn);
 }
 
 __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams p) {
-  extern __shared__ __align__(16) uint8_t dyn[];
+  extern __shared__ __align__(1024) uint8_t dyn[];
   const int tid = threadIdx.x;
   const int L = p.c.L;
   const int b = blockIdx.x;
@@ -443,29 +494,22 @@ __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams 
   commit_sequence(p.c, b, stopped, sm);
 }
 
-void choose_split(int R, int V, int dtype, int sm_count, int* S_out, int* chunk_out) {
-  const int target = dtype == DLLM_BF16 ? 16384 : 8192;  // 32 KB per CTA
-  const int smax = max_splits(V);
-  int S = std::max(1, (V + target - 1) / target);
-  // keep at least ~8 CTAs per SM in flight when there are few rows
-  while (static_cast<int64_t>(R) * S < static_cast<int64_t>(sm_count) * 8 && S * 2 <= smax &&
-         V / (S * 2) >= kMinChunk)
-    S *= 2;
-  S = std::min(S, smax);
-  int chunk = static_cast<int>(align_up((V + S - 1) / S, 8));
-  S = (V + chunk - 1) / chunk;
-  *S_out = S;
+// One 4 KB warp slice per item.
+void choose_split(int V, int dtype, int* S_out, int* chunk_out) {
+  const int chunk = dtype == DLLM_BF16 ? slice_elems<DLLM_BF16>() : slice_elems<DLLM_F32>();
+  *S_out = (V + chunk - 1) / chunk;
   *chunk_out = chunk;
 }
 
 }  // namespace
 
-int max_splits(int V) { return std::max(1, std::min(kMaxSplits, (V + kMinChunk - 1) / kMinChunk)); }
+// Upper bound of the slices per row over both dtypes (fp32 slices hold 1024 elements).
+int max_splits(int V) { return std::max(1, (V + 1023) / 1024); }
 
 size_t stats_ws_bytes(int B, int L, int V) {
   const size_t R = static_cast<size_t>(B) * L;
   const size_t parts = R * max_splits(V);
-  return kWsHeader + align_up(sizeof(int32_t) * B, 256) + 3 * align_up(4 * parts, 256);
+  return kWsHeader + 3 * align_up(4 * parts, 256);
 }
 
 StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
@@ -474,8 +518,6 @@ StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
   StatsWs w;
   w.status = reinterpret_cast<int32_t*>(p);
   p += kWsHeader;
-  w.counters = reinterpret_cast<int32_t*>(p);
-  p += align_up(sizeof(int32_t) * B, 256);
   w.part_m = reinterpret_cast<float*>(p);
   p += align_up(4 * parts, 256);
   w.part_s = reinterpret_cast<float*>(p);
@@ -494,8 +536,7 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   p.logits = static_cast<const char*>(logits);
   p.row_stride_bytes = sh.row_stride * es;
   p.V = sh.V;
-  choose_split(R, sh.V, sh.dtype, sm_count, &p.S, &p.chunk);
-  p.vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (p.row_stride_bytes % 16 == 0);
+  choose_split(sh.V, sh.dtype, &p.S, &p.chunk);
   p.stats = stats;
   p.ws = ws;
   p.c.B = sh.B;
@@ -509,13 +550,27 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
     p.masked = state->masked;
     p.eos_hit = state->eos_hit;
   }
-  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(R) * p.S));
-  const size_t smem = epi_smem_bytes(sh.L);
+  (void)sm_count;
+  const int64_t items = static_cast<int64_t>(R) * p.S;
+  const dim3 grid1(static_cast<unsigned>((items + kThreads / 32 - 1) / (kThreads / 32)));
   if (sh.dtype == DLLM_BF16)
-    stats_commit_kernel<DLLM_BF16><<<grid, kThreads, smem, stream>>>(p);
+    stats_partials_kernel<DLLM_BF16><<<grid1, kThreads, 0, stream>>>(p);
   else
-    stats_commit_kernel<DLLM_F32><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+    stats_partials_kernel<DLLM_F32><<<grid1, kThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the merge + commit kernel, one CTA per sequence, as a programmatic dependent launch
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sh.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = epi_smem_bytes(sh.L);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_commit_kernel, p);
 }
 
 cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,

@@ -33,9 +33,9 @@
  *    recorded in the status word at the start of the workspace; dllm_get_status reads it.
  *  - Workspace: `ws` points to at least dllm_workspace_bytes(shape) bytes (or
  *    dllm_smooth_workspace_bytes for dllm_smooth_embed), 256-byte aligned, zero-filled ONCE
- *    before its first use.  The kernels leave their counters at zero when they finish, so the
- *    same workspace serves any number of later calls on one stream.  Calls that run at the
- *    same time must use different workspaces.
+ *    before its first use (its first 4 bytes are the status word).  The same workspace serves
+ *    any number of later calls on one stream.  Calls that run at the same time must use
+ *    different workspaces.
  *
  * Data layout (row r = b*L + i is position i of sequence b):
  *  - logits: B*L rows of V elements, row r starting at element r*row_stride.  The pointer is
@@ -167,14 +167,16 @@ dllm_status dllm_commit_credit(const void* logits, const dllm_shape* shape,
 
 /*
  * Re-lay the embedding table once for the smoothing GEMM: E [V, d] bf16 row-major (the usual
- * table) -> Et [d, ldt] bf16, Et[c, v] = E[v, c], with ldt = V rounded up to a multiple of 8
- * (the pad columns are zeroed).  Bit patterns are copied unchanged.  d % 16 == 0.
+ * table) -> Et, the transpose stored K-slab-blocked: Et[(v / 64) * d + c][v % 64] = E[v][c], so
+ * that each 64-wide slab of the vocabulary is contiguous for every column c; slab entries with
+ * v >= V are zero.  dllm_embedding_t_elems(V, d) = d * (V rounded up to 64) elements.  Bit
+ * patterns are copied unchanged.  d % 16 == 0.  Et must be 16-byte aligned.
  */
 size_t dllm_embedding_t_elems(int32_t V, int32_t d);
 dllm_status dllm_prepare_embedding(const uint16_t* E, int32_t V, int32_t d, uint16_t* Et,
                                    dllm_stream_t stream);
 
-/* Bytes of workspace dllm_smooth_embed needs (the bf16 probability rows and counters). */
+/* Bytes of workspace dllm_smooth_embed needs (status word, bf16 probability rows, partials). */
 size_t dllm_smooth_workspace_bytes(const dllm_shape* shape, int32_t d);
 
 /*

@@ -13,6 +13,10 @@ import oracle
 import synth
 
 MARGIN = 1e-3
+# Credits carry state across steps, so redrawing one step cannot move a near-tie between two
+# stored credits; the eviction guard uses 1e-4 relative, 20x the worst-case fp32 drift of a
+# credit over 24 decay-and-add updates (~5e-6 relative).
+EVICT_MARGIN = 1e-4
 RTOL = 2e-3
 
 
@@ -45,9 +49,12 @@ def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray) -
             if not np.any(c > w.tau) and not _gap_ok(c):
                 return False
         elif w.strategy == "hierarchical":
-            if np.any(np.abs(c - float(np.float32(w.tau_low))) < MARGIN):
+            tl = float(np.float32(w.tau_low))
+            if np.any(np.abs(c - tl) < MARGIN):
                 return False
-            if not _gap_ok(c):  # the fallback may be taken; keep its pick unambiguous
+            # an eligible position always commits in its leaf, so the fallback runs only when
+            # no masked position is eligible
+            if not np.any(c >= tl) and not _gap_ok(c):
                 return False
         elif w.strategy == "credit":
             s = scores[b][m]
@@ -60,7 +67,7 @@ def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray) -
                 if argmax[b, i] in ids or (ids == -1).any():
                     continue
                 cr = np.sort(st.cand_credit[b, i])
-                if cr[1] - cr[0] < MARGIN * max(cr[1], 1e-30):
+                if cr[1] - cr[0] < EVICT_MARGIN * max(cr[1], 1e-30):
                     return False
     return True
 

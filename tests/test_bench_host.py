@@ -1,0 +1,60 @@
+"""Host-side logic of bench.py: rank seeding and max-over-ranks timing with gloo (world size 2,
+CPU only), and the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    r, w, _ = bench.dist_setup(world)
+    assert (r, w) == (rank, world)
+    bench.barrier(w)
+    slowest = bench.max_over_ranks(1.0 + r, w)  # rank 1 is "slower"
+    out[rank] = (bench.rank_seed(1004, r), slowest)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_ranks_shard_by_seed_and_report_the_slowest():
+    world, port = 2, _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_worker, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    seeds = {out[r][0] for r in range(world)}
+    assert len(seeds) == world           # independent batches per rank
+    assert all(out[r][1] == 2.0 for r in range(world))  # every rank sees the max
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["unit"] == "block-iters/s"

@@ -13,11 +13,12 @@ import diffusion_decoding_gb300 as dd
 pytestmark = pytest.mark.gpu
 
 
-def smooth_close(g: np.ndarray, o: np.ndarray, rtol=2e-3) -> None:
-    """Per element |g-o| <= rtol*max(|o|, 1e-2*max_row|o|); per row relative L2 <= rtol."""
+def smooth_close(g: np.ndarray, o: np.ndarray, scale: np.ndarray, rtol=2e-3) -> None:
+    """Per element |g-o| <= rtol * sum_v P_v |E_v,c| (the magnitude of the terms summed: an
+    entry that is a near-cancelling sum has no meaningful relative error of its own); per row
+    relative L2 <= rtol."""
     g = np.asarray(g, np.float64)
-    floor = 1e-2 * np.abs(o).max(axis=1, keepdims=True)
-    bound = rtol * np.maximum(np.abs(o), floor)
+    bound = rtol * scale
     bad = np.abs(g - o) > bound
     assert not bad.any(), f"{bad.sum()} elements outside the bound; worst " \
                           f"{np.max(np.abs(g - o) / np.maximum(bound, 1e-30)):.3g}x"
@@ -72,8 +73,10 @@ def _smooth_case(w, seed, calibrated, sample_rows=None):
     assert np.isnan(o[Mg:]).all(), "rows >= M must stay untouched"
     js = np.arange(Mg) if sample_rows is None else np.unique(
         np.linspace(0, Mg - 1, sample_rows).astype(int))
-    ref = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids_ref[js].astype(np.int32), E)
-    smooth_close(o[js], ref)
+    ids = ids_ref[js].astype(np.int32)
+    ref = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids, E)
+    scale = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids, E & np.uint16(0x7FFF))
+    smooth_close(o[js], ref, scale)
     return Mg
 
 
@@ -111,12 +114,15 @@ def test_smooth_skips_when_nothing_is_masked():
     assert int(M.item()) == 0 and (row_ids.cpu() == -1).all() and (out.cpu() == 7.0).all()
 
 
-def test_embedding_relayout_is_a_transpose():
+def test_embedding_relayout_is_a_blocked_transpose():
     V, d = 1001, 48
     E, Et = _table(V, d)
-    ldt = dd.dllm_embedding_t_elems(V, d) // d
-    et = Et.cpu().numpy().view(np.uint16).reshape(d, ldt)
-    assert np.array_equal(et[:, :V], E.T) and (et[:, V:] == 0).all()
+    Vp = dd.dllm_embedding_t_elems(V, d) // d
+    assert Vp == 1024
+    # Et[(v // 64) * d + c][v % 64] = E[v][c]
+    et = Et.cpu().numpy().view(np.uint16).reshape(Vp // 64, d, 64)
+    full = et.transpose(1, 0, 2).reshape(d, Vp)
+    assert np.array_equal(full[:, :V], E.T) and (full[:, V:] == 0).all()
 
 
 @pytest.mark.parametrize("B,L,P,w", [(1, 1, 0, 0), (3, 64, 1024, 4), (2, 300, 5, 9),
