@@ -77,6 +77,10 @@ _SIGS = {
     "dllm_kv_refresh_mask": (_c_i32, [ctypes.POINTER(dllm_block_state), _c_i32, _c_i32, _c_i32,
                                       _c_i32, _c_vp, _c_vp, _c_vp, _c_vp]),
     "dllm_get_status": (_c_i32, [_c_vp, _c_vp, ctypes.POINTER(_c_i32)]),
+    "dllm_commit_threshold_static": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape),
+                                              ctypes.POINTER(dllm_stats),
+                                              ctypes.POINTER(dllm_block_state), _c_f32, _c_i32,
+                                              _c_vp]),
 }
 
 _lib = None
@@ -277,6 +281,17 @@ def dllm_kv_refresh_mask(state: BlockState, prefix_len: int, window: int, refres
     _check(lib().dllm_kv_refresh_mask(ctypes.byref(bs), state.B, state.L, prefix_len, window,
                                       _ptr(refresh), _ptr(idx), _ptr(count), _stream(stream)),
            "dllm_kv_refresh_mask")
+
+
+def dllm_commit_threshold_static(logits, shape, stats: StatsBuffers, state: BlockState, tau: float,
+                                 eos_id: int, stream=None) -> None:
+    """dllm_commit_threshold for callers that cannot allocate: no workspace argument, the
+    scratch is a fixed static array inside the library (see include/dllm.h)."""
+    st, bs = stats.c(), state.c()
+    _check(lib().dllm_commit_threshold_static(_ptr(logits), ctypes.byref(shape),
+                                              ctypes.byref(st), ctypes.byref(bs), tau, eos_id,
+                                              _stream(stream)),
+           "dllm_commit_threshold_static")
 
 
 def dllm_get_status(ws, stream=None) -> int:

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdllm.so")
-SOURCES = ["stats_commit.cu", "scan.cu", "smooth.cu", "abi.cu"]
+SOURCES = ["stats_commit.cu", "scan.cu", "smooth.cu", "abi.cu", "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -231,6 +231,29 @@ dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32
                                  int32_t* idx, int32_t* count, dllm_stream_t stream);
 
 /*
+ * dllm_commit_threshold without a workspace argument, for callers that cannot allocate device
+ * memory where they decode (a serving runtime that reserves all memory up front and forbids
+ * allocation while requests are in flight, a plugin whose host framework owns every device
+ * buffer).  The pages have no counterpart to this call; it exists for those callers only.
+ * Same arguments (minus ws), same results and same errors as dllm_commit_threshold with
+ * logits != NULL, computed by the same kernel.  Its scratch is one static array of
+ * DLLM_STATIC_WORKSPACE_BYTES in device memory, part of the library image: every GPU that loads
+ * the library holds it until the process exits.
+ *  - Shapes whose dllm_workspace_bytes exceeds DLLM_STATIC_WORKSPACE_BYTES are rejected with
+ *    DLLM_ERR_UNSUPPORTED (4 MiB: e.g. B*L up to 16384 rows at V = 126464).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *    that device current; make that first call before any stream capture.
+ *  - Each call clears the array's status word on `stream`; nothing is allocated or freed.  All calls share the one array and it keeps the last call's contents, so calls
+ *    that overlap on the GPU (different streams, or concurrent graphs) race: serialise them.
+ *  - dllm_get_status cannot be used on this scratch; a fault inside the kernel still surfaces
+ *    as wrong results only, as for any call whose status word is never read.
+ */
+#define DLLM_STATIC_WORKSPACE_BYTES ((size_t)4 << 20)
+dllm_status dllm_commit_threshold_static(const void* logits, const dllm_shape* shape,
+                                         const dllm_stats* stats, const dllm_block_state* state,
+                                         float tau, int32_t eos_id, dllm_stream_t stream);
+
+/*
  * Read the device status word of a workspace (its first 4 bytes; synchronises `stream`).
  * *out_host receives DLLM_OK or the first fault a kernel recorded there (DLLM_ERR_TIMEOUT);
  * the word is then reset to DLLM_OK.  Works for both kinds of workspace.
