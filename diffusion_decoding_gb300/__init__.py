@@ -77,6 +77,7 @@ _SIGS = {
     "dllm_kv_refresh_mask": (_c_i32, [ctypes.POINTER(dllm_block_state), _c_i32, _c_i32, _c_i32,
                                       _c_i32, _c_vp, _c_vp, _c_vp, _c_vp]),
     "dllm_get_status": (_c_i32, [_c_vp, _c_vp, ctypes.POINTER(_c_i32)]),
+    "dllm_selftest_wait_timeout": (_c_i32, [_c_vp, ctypes.c_uint32, _c_vp]),
     "dllm_commit_threshold_static": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape),
                                               ctypes.POINTER(dllm_stats),
                                               ctypes.POINTER(dllm_block_state), _c_f32, _c_i32,
@@ -292,6 +293,11 @@ def dllm_commit_threshold_static(logits, shape, stats: StatsBuffers, state: Bloc
                                               ctypes.byref(st), ctypes.byref(bs), tau, eos_id,
                                               _stream(stream)),
            "dllm_commit_threshold_static")
+
+
+def dllm_selftest_wait_timeout(ws, limit_us: int, stream=None) -> None:
+    _check(lib().dllm_selftest_wait_timeout(_ptr(ws), limit_us, _stream(stream)),
+           "dllm_selftest_wait_timeout")
 
 
 def dllm_get_status(ws, stream=None) -> int:

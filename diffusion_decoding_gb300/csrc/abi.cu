@@ -313,6 +313,17 @@ dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32
   return ok();
 }
 
+dllm_status dllm_selftest_wait_timeout(void* ws, uint32_t limit_us, dllm_stream_t stream) {
+  DLLM_TRY(check_ws(ws));
+  if (limit_us < 1 || limit_us > 2000000)
+    return fail(DLLM_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
+  cudaError_t e = dllm::launch_wait_timeout_selftest(static_cast<int32_t*>(ws),
+                                                     static_cast<uint64_t>(limit_us) * 1000,
+                                                     reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_selftest_wait_timeout");
+  return ok();
+}
+
 dllm_status dllm_get_status(void* ws, dllm_stream_t stream, int32_t* out_host) {
   DLLM_TRY(check_ws(ws));
   if (!out_host) return fail(DLLM_ERR_INVALID_ARG, "out_host is null");

@@ -30,6 +30,7 @@ struct CommitArgs {
 // Stats/commit workspace layout.
 struct StatsWs {
   int32_t* status;
+  int32_t* row_cnt;   // [R] slices finished per row (re-armed to zero by the kernel)
   float* part_m;      // [R * S_max]
   float* part_s;
   int32_t* part_i;
@@ -84,6 +85,9 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
 cudaError_t launch_smooth_gemm(const SmoothPlan& plan, const uint16_t* P, const uint16_t* Et,
                                int ldt, float* out, const int32_t* M, void* ws,
                                cudaStream_t stream, const char** why);
+
+cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns,
+                                         cudaStream_t stream);
 
 // Record a message for dllm_last_error() on this thread (with a CUDA error string if e != 0).
 void set_last_error(const char* msg, cudaError_t e);

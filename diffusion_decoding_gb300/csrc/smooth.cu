@@ -5,12 +5,13 @@
 // Two launches: prob_rows_kernel writes the bf16 probability rows P (compacted), then
 // smooth_gemm_kernel contracts P with the embedding table on the 5th-generation tensor cores.
 // Both operands are stored K-slab-blocked, [ceil(V/64)][rows][64]: the 64-wide K slab of every
-// row is contiguous, so each 128-row TMA box is one contiguous 16 KB block (with K = V = 126464
-// a plain row-major box would touch a different memory page in every row).  TMA brings the
-// boxes (128-byte swizzle) into a multi-stage shared-memory ring; tcgen05.mma accumulates in
-// TMEM; epilogue warps read the accumulator back with tcgen05.ld.
-#include <cuda.h>
-
+// row is contiguous, so the 128 rows a CTA needs from one slab are one contiguous 16 KB run.
+// Producer warps copy those runs with 16-byte cp.async into a multi-stage shared-memory ring in
+// the 128-byte-swizzled layout; tcgen05.mma accumulates in TMEM; epilogue warps read the
+// accumulator back with tcgen05.ld.  (Tensor-map bulk copies were measured first: on this part
+// the copies of one CTA, consecutive K slabs of the same rows, completed one after another about
+// 0.8 us apart, capping the GEMM near 500 TFLOP/s; many warps issuing 16-byte copies do not
+// serialise that way.)
 #include <algorithm>
 
 #include "common.cuh"
@@ -33,11 +34,6 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -50,18 +46,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Box (0, y, slab) of a K-slab-blocked operand: rows y.. of one 64-wide K slab.
-__device__ __forceinline__ void tma_load_slab(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                              int y, int slab) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(y), "r"(slab)
-      : "memory");
+// 16-byte asynchronous global -> shared copy (LSU path; bypasses L1).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Tensor-memory allocation for a CTA pair: one warp in EACH of the two CTAs executes these
-// collectively; both CTAs receive the same column base.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (tcgen05).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Copy `rows` rows of one 64-wide K slab (rows of 128 B, contiguous in the K-slab-blocked
+// layout) into shared memory in the 128-byte-swizzled K-major layout tcgen05 descriptors read:
+// 16-byte chunk c of row i lands at i * 128 + ((c ^ (i & 7)) * 16).  One warp, coalesced.
+__device__ __forceinline__ void copy_slab_rows(uint32_t dst, const uint16_t* src, int rows,
+                                               int lane) {
+  const char* g = reinterpret_cast<const char*>(src);
+  const int chunks = rows * 8;
+  for (int j = lane; j < chunks; j += 32) {
+    const int i = j >> 3, c = j & 7;
+    cp_async16(dst + i * 128 + ((c ^ (i & 7)) << 4), g + static_cast<size_t>(j) * 16);
+  }
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
@@ -156,7 +171,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows 128 B apart,
-// 8-row groups 1024 B apart (the layout a 128-byte-swizzled TMA box of 64 bf16 columns writes).
+// 8-row groups 1024 B apart: 16-byte chunk c of row i at i * 128 + ((c ^ (i & 7)) * 16).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
@@ -175,23 +190,29 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
-// Bounded wait on an mbarrier phase.  On timeout: raise the CTA's abort flag and record
-// DLLM_ERR_TIMEOUT in the workspace status word; every other waiter then gives up too.
+// Bounded wait on an mbarrier phase.  The fast path is a plain try_wait spin; the clock and the
+// CTA's abort flag are consulted only every 1024 polls (reading them on every poll lengthened
+// each producer/consumer hand-off by microseconds).  On timeout: raise the CTA's abort flag and
+// record DLLM_ERR_TIMEOUT in the workspace status word; every other waiter then gives up too.
 template <bool kCluster = false>
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                         int32_t* status) {
+                         int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
   auto probe = [&]() {
     return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
-  if (probe()) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  uint64_t t0 = 0;
+  for (uint32_t spins = 0;; ++spins) {
     if (probe()) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      set_status(status, DLLM_ERR_TIMEOUT);
-      return false;
+    if ((spins & 1023u) == 1023u) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
+        *abort_flag = 1;
+        set_status(status, DLLM_ERR_TIMEOUT);
+        return false;
+      }
     }
   }
 }
@@ -203,13 +224,29 @@ __device__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing ever arrives at;
+// after limit_ns the wait gives up and records DLLM_ERR_TIMEOUT in the status word.
+__global__ void wait_timeout_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bar(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+}
+
 // ------------------------------------------------------------------ GEMM
 
 constexpr int kBM = 128;   // rows per CTA; a CTA pair covers 256
 constexpr int kBK = 64;    // one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;
-constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 TMEM + MMA (leader) / forwarder (peer),
-                                   // warps 2-5 epilogue
+constexpr int kGemmThreads = 256;  // warp 0: TMEM + MMA (leader) / forwarder (peer);
+                                   // warps 1-7: producers, one ring stage each;
+                                   // warps 4-7 then drain the accumulator (epilogue)
+constexpr int kProducers = 7;
 constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kMaxStages = 8;
 
@@ -229,21 +266,23 @@ struct GemmParams {
   float* part;         // [split_k, R_pad, d] otherwise
   const int32_t* M;
   int32_t* status;
+  const uint16_t* P;   // K-slab-blocked [slabs][R_pad][64]
+  const uint16_t* Et;  // K-slab-blocked [slabs][d][64]
 };
 
 // One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
-// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep TMA
-// ring.  The peer CTA forwards each landed stage to the leader's "full" barrier; the leader's
-// MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each stage's
-// release, and finally the accumulator-ready signal, to both CTAs.
+// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring;
+// every stage has its own producer warp (seven of them), which copies the stage with 16-byte
+// cp.async, waits for its copies, fences them to the async proxy and arrives.  The
+// peer CTA forwards each landed stage to the leader's "full" barrier; the leader's MMA thread
+// issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each stage's release, and
+// finally the accumulator-ready signal, to both CTAs.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
-    smooth_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    smooth_gemm_kernel(GemmParams p) {
   extern __shared__ uint8_t dyn_raw[];
   __shared__ uint64_t bars[2 * kMaxStages + 1];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int k_consumed;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -264,6 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int kb0 = ks * p.kb_per_split;
   const int nkb = max(0, min(p.num_kb, kb0 + p.kb_per_split) - kb0);
   const int S = p.stages;
+  const int P = min(S, kProducers);
   const uint32_t b_half_bytes = static_cast<uint32_t>(p.bn_max / 2) * kBK * 2;
 
   const uint32_t raw = smem_u32(dyn_raw);
@@ -282,10 +322,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(acc_bar, 1);
     abort_flag = 0;
-    k_consumed = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 0) {
     tmem_alloc_pair(smem_u32(&tmem_slot), p.tmem_cols);
     tmem_relinquish_pair();
   }
@@ -295,20 +334,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_v = &abort_flag;
-  int issued = 0;
+  const int prod = warp - 1;  // producer index of warps 1..7
 
-  if (warp == 0 && lane == 0) {
-    // ---- TMA producer (both CTAs): own 128 rows of P, own half of the E^T tile
-    for (int k = 0; k < nkb; ++k) {
+  if (warp >= 1 && prod < P) {
+    // ---- producers (both CTAs, whole warps): K blocks prod, prod + P, ... of own P rows and
+    // own half of the E^T tile, copied with 16-byte cp.async into the swizzled stage layout
+    const int bh = bn / 2;
+    for (int k = prod; k < nkb; k += P) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
-      if (!wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status)) break;
-      mbar_expect_tx(full0 + 8 * s, kATileBytes + b_half_bytes);
-      tma_load_slab(sA + s * kATileBytes, &tmA, full0 + 8 * s, my_m0, kb0 + k);
-      tma_load_slab(sB + s * b_half_bytes, &tmB, full0 + 8 * s, my_n0, kb0 + k);
-      issued = k + 1;
+      if (!__all_sync(kFull, wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status))) break;
+      const size_t slab = static_cast<size_t>(kb0 + k);
+      copy_slab_rows(sA + s * kATileBytes, p.P + (slab * p.R_pad + my_m0) * 64, kBM, lane);
+      copy_slab_rows(sB + s * b_half_bytes, p.Et + (slab * p.d + my_n0) * 64, bh, lane);
+      cp_async_wait_all();
+      fence_proxy_async_smem();  // the tensor core reads the stage through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(full0 + 8 * s);
     }
-  } else if (warp == 1 && lane == 0 && !leader) {
+  } else if (warp == 0 && lane == 0 && !leader) {
     // ---- forwarder (peer): tell the leader when each of this CTA's stages has landed
     const uint32_t leader_full0 = map_to_rank(full0, 0);
     for (int k = 0; k < nkb; ++k) {
@@ -317,7 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
       mbar_arrive_remote(leader_full0 + 8 * s);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 0 && lane == 0) {
     // ---- MMA issuer (leader)
     const uint32_t idesc = idesc_bf16(2 * kBM, bn);
     int k = 0;
@@ -335,10 +379,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
       umma_commit_pair(empty0 + 8 * s);  // stage s is free in both CTAs once these MMAs read it
     }
-    k_consumed = k;
     umma_commit_pair(acc_bar);  // accumulators complete in both CTAs
-  } else if (warp >= 2) {
+  }
+  if (warp >= 4) {
     // ---- epilogue (both CTAs): this CTA's 128 accumulator rows, TMEM -> registers -> global
+    __syncwarp();
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int row = my_m0 + q * 32 + lane;
     // warp-uniform: tcgen05.ld below is a .sync.aligned warp instruction
@@ -369,15 +414,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_v) {
-    // drain: copies already issued and MMAs already issued must land before smem/TMEM go away
-    if (warp == 0 && lane == 0) {
-      for (int k = k_consumed; k < issued; ++k) drain_bar(full0 + 8 * (k % S), (k / S) & 1);
-    }
-    if (warp == 1 && lane == 0) drain_bar(acc_bar, 0);
+    // drain: MMAs already issued must finish before smem/TMEM go away (each producer warp
+    // waited for its own copies before arriving)
+    if (warp == 0 && lane == 0) drain_bar(acc_bar, 0);
     __syncthreads();
   }
   cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may still touch it
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, p.tmem_cols);
   }
@@ -481,39 +524,6 @@ __global__ void transpose_bf16_kernel(const uint16_t* E, int V, int d, uint16_t*
 
 // ------------------------------------------------------------------ host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// K-slab-blocked bf16 operand [slabs][rows][64] as a 3-D tensor map; boxes of 64 x box_rows x 1
-// with 128-byte swizzle (the K-major layout tcgen05 descriptors expect).
-bool make_slab_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t slabs,
-                   uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {64, rows, slabs};
-  cuuint64_t strides[2] = {128, rows * 128};
-  cuuint32_t box[3] = {64, box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr size_t kMaxDynSmem = 227 * 1024;
 
 }  // namespace
@@ -554,6 +564,7 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
   }
   const size_t stage_bytes = kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2;
   pl.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage_bytes));
+  pl.stages = std::min(pl.stages, kProducers);  // one producer warp per stage
   const int R_pad = pl.m_tiles * kBM;
   size_t off = kWsHeader;
   off = align_up(off, 1024);
@@ -593,14 +604,8 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
                                int ldt, float* out, const int32_t* M, void* ws,
                                cudaStream_t stream, const char** why) {
   const int R_pad = pl.m_tiles * kBM;
-  CUtensorMap tmA, tmB;
-  const uint64_t slabs = static_cast<uint64_t>(pl.ldp) / 64;
   (void)ldt;
-  if (!make_slab_map(&tmA, P, R_pad, slabs, kBM) ||
-      !make_slab_map(&tmB, Et, pl.d, slabs, pl.bn_max / 2)) {
-    *why = "cuTensorMapEncodeTiled failed or is unavailable";
-    return cudaErrorInvalidValue;
-  }
+  (void)why;
   GemmParams gp{};
   gp.num_kb = (pl.V + kBK - 1) / kBK;
   gp.n_tiles = pl.n_tiles;
@@ -620,6 +625,8 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_part);
   gp.M = M;
   gp.status = static_cast<int32_t*>(ws);
+  gp.P = P;
+  gp.Et = Et;
   const size_t smem = static_cast<size_t>(pl.stages) *
                           (kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2) + 1024;
   cudaError_t e = cudaFuncSetAttribute(smooth_gemm_kernel,
@@ -628,11 +635,17 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   if (e != cudaSuccess) return e;
   // m_tiles = 2 x row pairs: one CTA per 128 rows, clusters of 2 along x
   const dim3 grid(static_cast<unsigned>(pl.m_tiles * pl.n_tiles * pl.split_k));
-  smooth_gemm_kernel<<<grid, kGemmThreads, smem, stream>>>(tmA, tmB, gp);
+  smooth_gemm_kernel<<<grid, kGemmThreads, smem, stream>>>(gp);
   e = cudaGetLastError();
   if (e != cudaSuccess || pl.split_k == 1) return e;
   splitk_reduce_kernel<<<std::min(1024, std::max(1, pl.R * pl.d / 4 / 256)), 256, 0, stream>>>(
       gp.part, pl.split_k, R_pad, pl.d, M, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns,
+                                         cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

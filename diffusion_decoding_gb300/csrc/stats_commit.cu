@@ -5,10 +5,13 @@
 //    front (8 per lane), takes the slice maximum with warp shuffles, sums exp(z - max) against
 //    that single maximum (no rescaling), finds the first index of the maximum, and writes one
 //    partial (max, sum, argmax).  Warps never wait for one another: no block barrier, no atomic.
-// 2. merge_commit_kernel (one CTA per sequence, chained with programmatic dependent launch so it
-//    is resident before the first kernel drains): merges the L x S partials of its sequence into
-//    the row statistics and runs the commit decision in shared memory (threshold, hierarchical
-//    or credit decoding; dInfer explainer, decoding-strategy component, methods 1-3).
+//    The warp that completes a row (one acquire/release atomic per slice on the row's counter)
+//    merges that row's partials and writes its statistics, overlapped with the other warps'
+//    streaming.
+// 2. commit_only_kernel (one CTA per sequence, chained with programmatic dependent launch so it
+//    is resident before the first kernel drains): reads the statistics of its sequence and runs
+//    the commit decision in shared memory (threshold, hierarchical or credit decoding; dInfer
+//    explainer, decoding-strategy component, methods 1-3).
 #include <algorithm>
 #include <climits>
 
@@ -72,6 +75,26 @@ constexpr int slice_elems() {
   return 32 * kVecs * SliceTraits<DT>::VEC;
 }
 
+// packed fp32 pairs (one 64-bit register pair) for the fma.rn.f32x2 / add.rn.f32x2 pipes
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int DT>
 __device__ __forceinline__ float vec_max(const uint4& q) {
   if constexpr (DT == DLLM_BF16) {
@@ -97,9 +120,10 @@ __device__ __forceinline__ void unpack16(const uint4& q, float* x) {
 }
 
 // One warp reduces elements [e0, e0 + n) of a row (n <= slice_elems) to (max, sum of
-// exp(z - max), lowest index of max).  The slice maximum is taken first, then every lane sums
-// exp(z - max) against that single maximum; only lanes holding the maximum look for its index.
-// The result is valid in every lane.
+// exp(z - max), lowest index of max).  Pass 1 takes each lane's maximum and remembers the first
+// of its vectors that holds it; the warp maximum follows by shuffles.  Pass 2 sums
+// exp(z - max) against that single maximum (no rescaling).  Only lanes holding the maximum
+// look for its index, by re-reading that one vector.  The result is valid in every lane.
 template <int DT>
 __device__ __forceinline__ RowAcc warp_reduce_slice(const char* row, int64_t e0, int n) {
   using T = SliceTraits<DT>;
@@ -116,35 +140,54 @@ __device__ __forceinline__ RowAcc warp_reduce_slice(const char* row, int64_t e0,
   }
   const float xt = lane < ntail ? load_logit(row, DT, e0 + nvec * T::VEC + lane) : -INFINITY;
 
-  float tm = xt;
+  float tm = -INFINITY;
+  int bu = -1;  // first vector of this lane holding tm (kVecs: the tail element)
 #pragma unroll
-  for (int u = 0; u < kVecs; ++u) tm = fmaxf(tm, vec_max<DT>(q[u]));
+  for (int u = 0; u < kVecs; ++u) {
+    const float vm = vec_max<DT>(q[u]);
+    if (vm > tm) {
+      tm = vm;
+      bu = u;
+    }
+  }
+  if (xt > tm) {
+    tm = xt;
+    bu = kVecs;
+  }
   float m = tm;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
 
   const float mb = (m == -INFINITY) ? 0.f : m * kLog2e;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // exp2(x*log2e - mb) summed with packed fp32x2 FMA / ADD: two elements per instruction
+  const uint64_t k2 = pack2(kLog2e, kLog2e), nmb2 = pack2(-mb, -mb);
+  uint64_t acc2[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
 #pragma unroll
   for (int u = 0; u < kVecs; ++u) {
     float x[T::VEC];
     unpack16<DT>(q[u], x);
 #pragma unroll
-    for (int j = 0; j < T::VEC; ++j) acc[j & 3] += ex2(fmaf(x[j], kLog2e, -mb));
+    for (int j = 0; j < T::VEC; j += 2) {
+      float t0, t1;
+      unpack2(fma2(pack2(x[j], x[j + 1]), k2, nmb2), t0, t1);
+      acc2[(j >> 1) & 1] = add2(acc2[(j >> 1) & 1], pack2(ex2(t0), ex2(t1)));
+    }
   }
-  acc[0] += ex2(fmaf(xt, kLog2e, -mb));
-  float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  float a0, a1, a2, a3;
+  unpack2(acc2[0], a0, a1);
+  unpack2(acc2[1], a2, a3);
+  float sum = ((a0 + a1) + (a2 + a3)) + ex2(fmaf(xt, kLog2e, -mb));
   int idx = INT_MAX;
   if (tm == m && m != -INFINITY) {  // rare: this lane holds the slice maximum
-#pragma unroll
-    for (int u = kVecs - 1; u >= 0; --u) {
+    if (bu == kVecs) {
+      idx = nvec * T::VEC + lane;
+    } else {
+      const int vi = bu * 32 + lane;
       float x[T::VEC];
-      unpack16<DT>(q[u], x);
-#pragma unroll
+      unpack16<DT>(ld_stream_v4(base + static_cast<int64_t>(vi) * 16), x);
       for (int j = T::VEC - 1; j >= 0; --j)
-        if (x[j] == m) idx = (u * 32 + lane) * T::VEC + j;
+        if (x[j] == m) idx = vi * T::VEC + j;
     }
-    if (xt == m && idx == INT_MAX) idx = nvec * T::VEC + lane;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -378,71 +421,16 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
 
 // ------------------------------------------------------------------ kernels
 
-// Last CTA of sequence b: merge the L*S slice partials into row statistics, then decide the
-// commits.  Kept out of line so that its registers do not constrain the streaming loop.
-__device__ __noinline__ void sequence_epilogue(const FusedParams& p, int b, uint8_t* dyn) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nt = blockDim.x, nw = nt >> 5;
-  const int L = p.c.L;
-  const EpiSmem sm = carve(dyn, L);
-  const bool committing = p.c.ca.mode != kStatsOnly;
-  int any_masked = 0;
-  for (int i = tid; i < L; i += nt) {
-    const uint8_t m = p.masked ? p.masked[static_cast<int64_t>(b) * L + i] : 1;
-    sm.mask[i] = m;
-    any_masked |= m;
-  }
-  any_masked = __syncthreads_or(any_masked);
-  const bool stopped = committing && ((p.eos_hit && p.eos_hit[b]) || !any_masked);
-  // merge: each warp takes rows warp, warp+nw, ...; the partial loads of up to kRowBatch rows
-  // are issued together so the L2 round trips overlap
-  constexpr int kRowBatch = 8;
-  const int S = p.S;
-  for (int i0 = warp; i0 < L; i0 += nw * kRowBatch) {
-    RowAcc a[kRowBatch];
-#pragma unroll
-    for (int k = 0; k < kRowBatch; ++k) {
-      a[k] = row_acc_empty();
-      const int i = i0 + k * nw;
-      if (i >= L || !sm.mask[i] || stopped) continue;
-      const int64_t row = static_cast<int64_t>(b) * L + i;
-      for (int j = lane; j < S; j += 32) {
-        const int64_t pi = row * S + j;
-        RowAcc q{__ldcg(p.ws.part_m + pi), __ldcg(p.ws.part_s + pi), __ldcg(p.ws.part_i + pi)};
-        a[k] = row_acc_merge(a[k], q);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kRowBatch; ++k) {
-      const int i = i0 + k * nw;
-      const RowAcc t = row_acc_warp_reduce(a[k]);
-      if (lane == 0 && i < L) {
-        const int64_t row = static_cast<int64_t>(b) * L + i;
-        const bool act = sm.mask[i] && !stopped;
-        float rm = -INFINITY, l = -INFINITY, cf = 0.f;
-        int am = -1;
-        if (act) {
-          rm = t.m;
-          l = t.m + logf(t.s);
-          cf = 1.f / t.s;
-          am = t.idx;
-        }
-        p.stats.row_max[row] = rm;
-        p.stats.lse[row] = l;
-        p.stats.conf[row] = cf;
-        p.stats.argmax[row] = am;
-        sm.val[i] = cf;
-        sm.am[i] = am;
-      }
-    }
-  }
-  __syncthreads();
-  if (committing) commit_sequence(p.c, b, stopped, sm);
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams p) {
-  // let the merge kernel's CTAs become resident while this grid drains
+  // let the commit kernel's CTAs become resident while this grid drains
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp;
@@ -453,26 +441,49 @@ __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams
   const int sl = static_cast<int>(item - r * S);
   const bool active = (p.masked == nullptr || p.masked[r]) &&
                       !(p.eos_hit != nullptr && p.eos_hit[r / L]);
-  if (!active) return;  // the merge kernel never reads partials of rows that are not read
+  if (!active) {  // rows not read report -inf, -inf, 0, -1 (written once, by slice 0's warp)
+    if (sl == 0 && lane == 0) {
+      p.stats.row_max[r] = -INFINITY;
+      p.stats.lse[r] = -INFINITY;
+      p.stats.conf[r] = 0.f;
+      p.stats.argmax[r] = -1;
+    }
+    return;
+  }
   const int64_t e0 = static_cast<int64_t>(sl) * p.chunk;
   const int n = static_cast<int>(min(static_cast<int64_t>(p.V), e0 + p.chunk) - e0);
   const RowAcc a = warp_reduce_slice<DT>(p.logits + r * p.row_stride_bytes, e0, n);
+  // publish this slice's partial; the warp that completes the row merges all of its slices
+  int last = 0;
   if (lane == 0) {
     p.ws.part_m[item] = a.m;
     p.ws.part_s[item] = a.s;
     p.ws.part_i[item] = a.idx;
+    last = atomic_add_acq_rel(p.ws.row_cnt + r, 1) == S - 1;
   }
-}
-
-__global__ void __launch_bounds__(kThreads) merge_commit_kernel(FusedParams p) {
-  extern __shared__ __align__(1024) uint8_t dyn[];
-  // every partial, and every read of the block state, of the first kernel is complete
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  sequence_epilogue(p, blockIdx.x, dyn);
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+  RowAcc t = row_acc_empty();
+  for (int j = lane; j < S; j += 32) {
+    const int64_t pi = r * S + j;
+    t = row_acc_merge(t, RowAcc{__ldcg(p.ws.part_m + pi), __ldcg(p.ws.part_s + pi),
+                                __ldcg(p.ws.part_i + pi)});
+  }
+  t = row_acc_warp_reduce(t);
+  if (lane == 0) {
+    p.stats.row_max[r] = t.m;
+    p.stats.lse[r] = t.m + logf(t.s);
+    p.stats.conf[r] = 1.f / t.s;
+    p.stats.argmax[r] = t.idx;
+    p.ws.row_cnt[r] = 0;  // re-armed for the next launch on this workspace
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams p) {
   extern __shared__ __align__(1024) uint8_t dyn[];
+  // launched after the statistics kernel as a programmatic dependent launch (or plainly):
+  // wait until every statistic and every read of the block state there is complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x;
   const int L = p.c.L;
   const int b = blockIdx.x;
@@ -509,7 +520,7 @@ int max_splits(int V) { return std::max(1, (V + 1023) / 1024); }
 size_t stats_ws_bytes(int B, int L, int V) {
   const size_t R = static_cast<size_t>(B) * L;
   const size_t parts = R * max_splits(V);
-  return kWsHeader + 3 * align_up(4 * parts, 256);
+  return kWsHeader + align_up(4 * R, 256) + 3 * align_up(4 * parts, 256);
 }
 
 StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
@@ -518,6 +529,8 @@ StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
   StatsWs w;
   w.status = reinterpret_cast<int32_t*>(p);
   p += kWsHeader;
+  w.row_cnt = reinterpret_cast<int32_t*>(p);
+  p += align_up(4 * static_cast<size_t>(B) * L, 256);
   w.part_m = reinterpret_cast<float*>(p);
   p += align_up(4 * parts, 256);
   w.part_s = reinterpret_cast<float*>(p);
@@ -559,7 +572,11 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
     stats_partials_kernel<DLLM_F32><<<grid1, kThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // the merge + commit kernel, one CTA per sequence, as a programmatic dependent launch
+  if (ca.mode == kStatsOnly) return cudaSuccess;
+  // the commit kernel, one CTA per sequence, as a programmatic dependent launch
+  CommitOnlyParams cp{};
+  cp.stats = stats;
+  cp.c = p.c;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.B);
   cfg.blockDim = dim3(kThreads);
@@ -570,7 +587,7 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_commit_kernel, p);
+  return cudaLaunchKernelEx(&cfg, commit_only_kernel, cp);
 }
 
 cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,

@@ -231,6 +231,14 @@ dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32
                                  int32_t* idx, int32_t* count, dllm_stream_t stream);
 
 /*
+ * Self-test of failure detection (no counterpart in the pages): runs the bounded wait the
+ * smoothing GEMM uses on a barrier that nothing ever completes.  After limit_us microseconds
+ * (1 .. 2,000,000) the wait gives up and records DLLM_ERR_TIMEOUT in the status word of `ws`
+ * (any workspace, or 256 zeroed bytes); read it with dllm_get_status.  Nothing faults or hangs.
+ */
+dllm_status dllm_selftest_wait_timeout(void* ws, uint32_t limit_us, dllm_stream_t stream);
+
+/*
  * dllm_commit_threshold without a workspace argument, for callers that cannot allocate device
  * memory where they decode (a serving runtime that reserves all memory up front and forbids
  * allocation while requests are in flight, a plugin whose host framework owns every device
@@ -243,7 +251,8 @@ dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32
  *    DLLM_ERR_UNSUPPORTED (4 MiB: e.g. B*L up to 16384 rows at V = 126464).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *    that device current; make that first call before any stream capture.
- *  - Each call clears the array's status word on `stream`; nothing is allocated or freed.  All calls share the one array and it keeps the last call's contents, so calls
+ *  - Each call clears the array's status word and row counters on `stream`; nothing is
+ *    allocated or freed.  All calls share the one array and it keeps the last call's contents, so calls
  *    that overlap on the GPU (different streams, or concurrent graphs) race: serialise them.
  *  - dllm_get_status cannot be used on this scratch; a fault inside the kernel still surfaces
  *    as wrong results only, as for any call whose status word is never read.

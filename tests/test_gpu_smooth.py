@@ -142,3 +142,14 @@ def test_kv_refresh_random_patterns(B, L, P, w):
     assert np.array_equal(refresh.cpu().numpy().reshape(B, T), r)
     assert np.array_equal(idx.cpu().numpy().reshape(B, T), i)
     assert np.array_equal(count.cpu().numpy(), c)
+
+
+def test_bounded_wait_times_out_and_reports_status():
+    # a wait that nothing satisfies gives up after its limit and records DLLM_ERR_TIMEOUT; the
+    # context stays usable and the status word resets once read
+    ws = dd.workspace(256)
+    dd.dllm_selftest_wait_timeout(ws, 20000)  # 20 ms
+    assert dd.dllm_get_status(ws) == dd.DLLM_ERR_TIMEOUT
+    assert dd.dllm_get_status(ws) == dd.DLLM_OK
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum().item()) == 8.0
