@@ -243,7 +243,7 @@ __global__ void wait_timeout_selftest_kernel(int32_t* status, uint64_t limit_ns)
 constexpr int kBM = 128;   // rows per CTA; a CTA pair covers 256
 constexpr int kBK = 64;    // one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;
-constexpr int kGemmThreads = 256;  // warp 0: TMEM + MMA (leader) / forwarder (peer);
+constexpr int kGemmThreads = 256;  // warp 0: TMEM allocation + MMA issue (leader);
                                    // warps 1-7: producers, one ring stage each;
                                    // warps 4-7 then drain the accumulator (epilogue)
 constexpr int kProducers = 7;
@@ -273,10 +273,12 @@ struct GemmParams {
 // One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
 // stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring;
 // every stage has its own producer warp (seven of them), which copies the stage with 16-byte
-// cp.async, waits for its copies, fences them to the async proxy and arrives.  The
-// peer CTA forwards each landed stage to the leader's "full" barrier; the leader's MMA thread
-// issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each stage's release, and
-// finally the accumulator-ready signal, to both CTAs.
+// cp.async, waits for its copies, fences them to the async proxy and arrives on the leader
+// CTA's "full" barrier for that stage (the peer's producers arrive remotely, with cluster-scope
+// release; a single thread forwarding the peer's stages one by one cost ~0.7 us per stage,
+// because each cluster-scope release waits behind the copies in flight).  The leader's MMA
+// thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each stage's
+// release, and finally the accumulator-ready signal, to both CTAs.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     smooth_gemm_kernel(GemmParams p) {
   extern __shared__ uint8_t dyn_raw[];
@@ -316,7 +318,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      // leader: its own producer's expect-tx arrival + the peer's forwarded arrival
+      // leader: its own producer's arrival + the peer producer's remote arrival (the peer's
+      // full barriers are not used)
       mbar_init(full0 + 8 * s, leader ? 2 : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -340,6 +343,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     // ---- producers (both CTAs, whole warps): K blocks prod, prod + P, ... of own P rows and
     // own half of the E^T tile, copied with 16-byte cp.async into the swizzled stage layout
     const int bh = bn / 2;
+    // the peer's producers arrive on the leader's barrier directly (cluster-scope release):
+    // seven arrivals in flight at once instead of one forwarding thread serialising them
+    const uint32_t leader_full0 = map_to_rank(full0, 0);
     for (int k = prod; k < nkb; k += P) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
@@ -350,18 +356,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       cp_async_wait_all();
       fence_proxy_async_smem();  // the tensor core reads the stage through the async proxy
       __syncwarp();
-      if (lane == 0) mbar_arrive_local(full0 + 8 * s);
+      if (lane == 0) {
+        if (leader) mbar_arrive_local(full0 + 8 * s);
+        else mbar_arrive_remote(leader_full0 + 8 * s);
+      }
     }
-  } else if (warp == 0 && lane == 0 && !leader) {
-    // ---- forwarder (peer): tell the leader when each of this CTA's stages has landed
-    const uint32_t leader_full0 = map_to_rank(full0, 0);
-    for (int k = 0; k < nkb; ++k) {
-      const int s = k % S;
-      const uint32_t ph = (k / S) & 1;
-      if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
-      mbar_arrive_remote(leader_full0 + 8 * s);
-    }
-  } else if (warp == 0 && lane == 0) {
+  } else if (warp == 0 && lane == 0 && leader) {
     // ---- MMA issuer (leader)
     const uint32_t idesc = idesc_bf16(2 * kBM, bn);
     int k = 0;
