@@ -6,12 +6,11 @@
 // smooth_gemm_kernel contracts P with the embedding table on the 5th-generation tensor cores.
 // Both operands are stored K-slab-blocked, [ceil(V/64)][rows][64]: the 64-wide K slab of every
 // row is contiguous, so the 128 rows a CTA needs from one slab are one contiguous 16 KB run.
-// Producer warps copy those runs with 16-byte cp.async into a multi-stage shared-memory ring in
-// the 128-byte-swizzled layout; tcgen05.mma accumulates in TMEM; epilogue warps read the
-// accumulator back with tcgen05.ld.  (Tensor-map bulk copies were measured first: on this part
-// the copies of one CTA, consecutive K slabs of the same rows, completed one after another about
-// 0.8 us apart, capping the GEMM near 500 TFLOP/s; many warps issuing 16-byte copies do not
-// serialise that way.)
+// TMA (3-D tensor maps over the blocked layout, 128-byte swizzle) brings those runs into a
+// multi-stage shared-memory ring; tcgen05.mma accumulates in TMEM; epilogue warps read the
+// accumulator back with tcgen05.ld.
+#include <cuda.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -47,34 +46,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // 16-byte asynchronous global -> shared copy (LSU path; bypasses L1).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
+// TMA box (0, y, slab) of a K-slab-blocked operand (rows y.. of one 64-wide K slab) into this
+// CTA's shared memory.  .cta_group::2: the completion may be signalled on an mbarrier in either
+// CTA of the pair (`bar` is a shared::cluster address); both CTAs' boxes complete on the leader's
+// barrier, so no thread has to relay the peer's progress.
+__device__ __forceinline__ void tma_load_slab_pair(uint32_t dst, const CUtensorMap* map,
+                                                   uint32_t bar, int y, int slab) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(y), "r"(slab)
+      : "memory");
 }
 
-// Make this thread's generic-proxy shared-memory writes visible to the async proxy (tcgen05).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Copy `rows` rows of one 64-wide K slab (rows of 128 B, contiguous in the K-slab-blocked
-// layout) into shared memory in the 128-byte-swizzled K-major layout tcgen05 descriptors read:
-// 16-byte chunk c of row i lands at i * 128 + ((c ^ (i & 7)) * 16).  One warp, coalesced.
-__device__ __forceinline__ void copy_slab_rows(uint32_t dst, const uint16_t* src, int rows,
-                                               int lane) {
-  const char* g = reinterpret_cast<const char*>(src);
-  const int chunks = rows * 8;
-  for (int j = lane; j < chunks; j += 32) {
-    const int i = j >> 3, c = j & 7;
-    cp_async16(dst + i * 128 + ((c ^ (i & 7)) << 4), g + static_cast<size_t>(j) * 16);
-  }
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -103,12 +94,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-
-// Arrive (release, cluster scope) on an mbarrier that may live in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -251,6 +236,8 @@ constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kMaxStages = 8;
 
 struct GemmParams {
+  CUtensorMap tmA;    // P: K-slab-blocked [slabs][R_pad][64], boxes of 64 x 128 x 1
+  CUtensorMap tmB;    // E^T: K-slab-blocked [slabs][d][64], boxes of 64 x bn_max/2 x 1
   int num_kb;         // 64-wide K blocks over V
   int n_tiles;
   int bn_base;        // narrow pair-tile width; the first bn_rem tiles are 16 wider
@@ -266,21 +253,19 @@ struct GemmParams {
   float* part;         // [split_k, R_pad, d] otherwise
   const int32_t* M;
   int32_t* status;
-  const uint16_t* P;   // K-slab-blocked [slabs][R_pad][64]
-  const uint16_t* Et;  // K-slab-blocked [slabs][d][64]
 };
 
 // One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
-// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring;
-// every stage has its own producer warp (seven of them), which copies the stage with 16-byte
-// cp.async, waits for its copies, fences them to the async proxy and arrives on the leader
-// CTA's "full" barrier for that stage (the peer's producers arrive remotely, with cluster-scope
-// release; a single thread forwarding the peer's stages one by one cost ~0.7 us per stage,
-// because each cluster-scope release waits behind the copies in flight).  The leader's MMA
-// thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each stage's
-// release, and finally the accumulator-ready signal, to both CTAs.
+// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring.
+// Every stage has its own producer warp (seven of them): once the stage is free it issues the
+// stage's two TMA boxes in its CTA, and both CTAs' boxes complete on the leader CTA's "full"
+// barrier for that stage (the leader's producer posts the byte count of all four boxes).  The
+// leader's MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each
+// stage's release, and finally the accumulator-ready signal, to both CTAs.  No thread relays
+// progress across the pair: an earlier version in which the peer's stages were forwarded by a
+// cluster-scope release arrive spent ~0.7 us per stage on that hop.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
-    smooth_gemm_kernel(GemmParams p) {
+    smooth_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t dyn_raw[];
   __shared__ uint64_t bars[2 * kMaxStages + 1];
   __shared__ uint32_t tmem_slot;
@@ -318,9 +303,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      // leader: its own producer's arrival + the peer producer's remote arrival (the peer's
-      // full barriers are not used)
-      mbar_init(full0 + 8 * s, leader ? 2 : 1);
+      mbar_init(full0 + 8 * s, 1);  // the leader producer's expect-tx arrival (the peer's
+                                    // full barriers are not used)
       mbar_init(empty0 + 8 * s, 1);
     }
     mbar_init(acc_bar, 1);
@@ -339,27 +323,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_v = &abort_flag;
   const int prod = warp - 1;  // producer index of warps 1..7
 
+  int last_k = -1;  // this producer's last issued K block (drained after an abort)
   if (warp >= 1 && prod < P) {
-    // ---- producers (both CTAs, whole warps): K blocks prod, prod + P, ... of own P rows and
-    // own half of the E^T tile, copied with 16-byte cp.async into the swizzled stage layout
-    const int bh = bn / 2;
-    // the peer's producers arrive on the leader's barrier directly (cluster-scope release):
-    // seven arrivals in flight at once instead of one forwarding thread serialising them
+    // ---- producers (both CTAs): K blocks prod, prod + P, ... of own 128 P rows and own half
+    // of the E^T tile; whole warps wait, lane 0 issues
     const uint32_t leader_full0 = map_to_rank(full0, 0);
+    const uint32_t stage_tx = 2u * (kATileBytes + b_half_bytes);
+    if (lane == 0) {
+      prefetch_tensormap(&p.tmA);
+      prefetch_tensormap(&p.tmB);
+    }
     for (int k = prod; k < nkb; k += P) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
       if (!__all_sync(kFull, wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status))) break;
-      const size_t slab = static_cast<size_t>(kb0 + k);
-      copy_slab_rows(sA + s * kATileBytes, p.P + (slab * p.R_pad + my_m0) * 64, kBM, lane);
-      copy_slab_rows(sB + s * b_half_bytes, p.Et + (slab * p.d + my_n0) * 64, bh, lane);
-      cp_async_wait_all();
-      fence_proxy_async_smem();  // the tensor core reads the stage through the async proxy
-      __syncwarp();
       if (lane == 0) {
-        if (leader) mbar_arrive_local(full0 + 8 * s);
-        else mbar_arrive_remote(leader_full0 + 8 * s);
+        const int slab = kb0 + k;
+        if (leader) mbar_expect_tx(full0 + 8 * s, stage_tx);
+        tma_load_slab_pair(sA + s * kATileBytes, &p.tmA, leader_full0 + 8 * s, my_m0, slab);
+        tma_load_slab_pair(sB + s * b_half_bytes, &p.tmB, leader_full0 + 8 * s, my_n0, slab);
       }
+      last_k = k;
+      __syncwarp();
     }
   } else if (warp == 0 && lane == 0 && leader) {
     // ---- MMA issuer (leader)
@@ -368,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     for (; k < nkb; ++k) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
-      if (!wait_bar<true>(full0 + 8 * s, ph, abort_v, p.status)) break;
+      if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
       tc_fence_after();
       const uint32_t a_s = sA + s * kATileBytes;
       const uint32_t b_s = sB + s * b_half_bytes;
@@ -414,9 +399,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_v) {
-    // drain: MMAs already issued must finish before smem/TMEM go away (each producer warp
-    // waited for its own copies before arriving)
+    // drain (bounded): MMAs already issued must finish, and TMA boxes still in flight must
+    // land, before shared memory and TMEM go away.  Both CTAs' boxes complete on the leader's
+    // barriers, and the peer waits at the cluster barrier below until the leader has drained.
     if (warp == 0 && lane == 0) drain_bar(acc_bar, 0);
+    if (leader && last_k >= 0 && lane == 0) drain_bar(full0 + 8 * (last_k % S), (last_k / S) & 1);
     __syncthreads();
   }
   cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may still touch it
@@ -528,6 +515,45 @@ constexpr size_t kMaxDynSmem = 227 * 1024;
 
 }  // namespace
 
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (no libcuda link).
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
+  return fn;
+}
+
+// K-slab-blocked bf16 operand [slabs][rows][64] as a 3-D tensor map; boxes of 64 x box_rows x 1
+// with 128-byte swizzle (the K-major layout the tcgen05 descriptors expect).  Rows of a box
+// beyond `rows` read as zeros.
+bool make_slab_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t slabs,
+                   uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, slabs};
+  cuuint64_t strides[2] = {128, rows * 128};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
   SmoothPlan pl{};
   pl.R = B * L;
@@ -605,8 +631,13 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
                                cudaStream_t stream, const char** why) {
   const int R_pad = pl.m_tiles * kBM;
   (void)ldt;
-  (void)why;
   GemmParams gp{};
+  const uint64_t slabs = static_cast<uint64_t>(pl.ldp) / 64;
+  if (!make_slab_map(&gp.tmA, P, R_pad, slabs, kBM) ||
+      !make_slab_map(&gp.tmB, Et, pl.d, slabs, pl.bn_max / 2)) {
+    *why = "cuTensorMapEncodeTiled failed or is unavailable (E^T must be 16-byte aligned)";
+    return cudaErrorInvalidValue;
+  }
   gp.num_kb = (pl.V + kBK - 1) / kBK;
   gp.n_tiles = pl.n_tiles;
   const int units16 = pl.d / 16;
@@ -625,8 +656,6 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_part);
   gp.M = M;
   gp.status = static_cast<int32_t*>(ws);
-  gp.P = P;
-  gp.Et = Et;
   const size_t smem = static_cast<size_t>(pl.stages) *
                           (kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2) + 1024;
   cudaError_t e = cudaFuncSetAttribute(smooth_gemm_kernel,
