@@ -30,7 +30,6 @@ struct CommitArgs {
 // Stats/commit workspace layout.
 struct StatsWs {
   int32_t* status;
-  int32_t* row_cnt;   // [R] slices finished per row (re-armed to zero by the kernel)
   float* part_m;      // [R * S_max]
   float* part_s;
   int32_t* part_i;
@@ -40,8 +39,8 @@ int max_splits(int V);
 size_t stats_ws_bytes(int B, int L, int V);
 StatsWs stats_ws_layout(void* ws, int B, int L, int V);
 
-// Fused pass: streaming statistics (+ commit epilogue in the last CTA of each sequence).
-// masked may be null only in kStatsOnly mode (every row computed).
+// Streaming statistics (slice partials), then one CTA per sequence that merges them and, unless
+// in kStatsOnly mode, runs the commit.  masked may be null only in kStatsOnly mode (every row).
 cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const uint8_t* masked,
                                 const dllm_stats& stats, const dllm_block_state* state,
                                 const CommitArgs& ca, const StatsWs& ws, int sm_count,

@@ -5,8 +5,8 @@
 // a serving runtime that reserves all device memory up front in its own pool and forbids
 // allocation while requests are in flight, a plugin whose host framework owns every device
 // buffer, or code that must not take the device-wide synchronisation an allocation may imply.
-// For them this entry point takes no workspace argument: its scratch (status word, per-row slice
-// counters, slice partials) lives in one fixed-size array in device global memory that
+// For them this entry point takes no workspace argument: its scratch (status word, slice
+// partials) lives in one fixed-size array in device global memory that
 // is part of the library image, so every GPU that loads the library holds it until the process
 // exits.
 //
@@ -72,12 +72,10 @@ dllm_status dllm_commit_threshold_static(const void* logits, const dllm_shape* s
   void* ws = nullptr;
   dllm_status st = static_ws_address(&ws);
   if (st != DLLM_OK) return st;
-  // The status word and the per-row slice counters must start at zero: clear them (no
-  // allocation).  The partials need no clearing: every partial read is written by the call.
-  const size_t head =
-      dllm::kWsHeader + dllm::align_up(4 * static_cast<size_t>(shape->B) * shape->L, 256);
+  // The status word must start at zero: clear the header (no allocation).  The partials need no
+  // clearing: every partial read is written by the call.
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, head, s);
+  cudaError_t e = cudaMemsetAsync(ws, 0, dllm::kWsHeader, s);
   if (e != cudaSuccess) return fail(DLLM_ERR_CUDA, "clearing the static workspace", e);
   return dllm_commit_threshold(logits, shape, stats, state, tau, eos_id, ws, stream);
 }

@@ -4,14 +4,16 @@
 //    are cut into 4 KB slices; each warp owns one slice, issues all of its 128-bit loads up
 //    front (8 per lane), takes the slice maximum with warp shuffles, sums exp(z - max) against
 //    that single maximum (no rescaling), finds the first index of the maximum, and writes one
-//    partial (max, sum, argmax).  Warps never wait for one another: no block barrier, no atomic.
-//    The warp that completes a row (one acquire/release atomic per slice on the row's counter)
-//    merges that row's partials and writes its statistics, overlapped with the other warps'
-//    streaming.
+//    partial (max, sum, argmax).  Warps never wait for one another: no block barrier, no atomic,
+//    no fence.  (Completing each row inside this kernel, with an acquire/release atomic per
+//    slice on a row counter, cost ~17 us at 1024 rows x V = 126464: every warp's release fence
+//    waited behind the loads in flight.)
 // 2. commit_only_kernel (one CTA per sequence, chained with programmatic dependent launch so it
-//    is resident before the first kernel drains): reads the statistics of its sequence and runs
+//    is resident before the first kernel drains): merges the slice partials of its sequence's
+//    rows into their statistics (four threads per row, every load issued up front), then runs
 //    the commit decision in shared memory (threshold, hierarchical or credit decoding; dInfer
-//    explainer, decoding-strategy component, methods 1-3).
+//    explainer, decoding-strategy component, methods 1-3).  In statistics-only mode it only
+//    merges.
 #include <algorithm>
 #include <climits>
 
@@ -44,6 +46,12 @@ struct FusedParams {
 struct CommitOnlyParams {
   dllm_stats stats;
   CommitCtx c;
+  int S;                  // slices per row (1: the statistics are complete, nothing to merge)
+  const float* part_m;    // [R * S] slice partials
+  const float* part_s;
+  const int32_t* part_i;
+  const uint8_t* masked;  // rows that were read (null: all rows; statistics-only mode)
+  const int32_t* eos_hit; // null in statistics-only mode
 };
 
 // ------------------------------------------------------------------ slice reduction
@@ -421,11 +429,11 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
 
 // ------------------------------------------------------------------ kernels
 
-__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
+__device__ __forceinline__ void write_row_stats(const dllm_stats& st, int64_t r, const RowAcc& a) {
+  st.row_max[r] = a.m;
+  st.lse[r] = a.m + logf(a.s);
+  st.conf[r] = 1.f / a.s;
+  st.argmax[r] = a.idx;
 }
 
 template <int DT>
@@ -453,40 +461,65 @@ __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams
   const int64_t e0 = static_cast<int64_t>(sl) * p.chunk;
   const int n = static_cast<int>(min(static_cast<int64_t>(p.V), e0 + p.chunk) - e0);
   const RowAcc a = warp_reduce_slice<DT>(p.logits + r * p.row_stride_bytes, e0, n);
-  // publish this slice's partial; the warp that completes the row merges all of its slices
-  int last = 0;
-  if (lane == 0) {
+  if (lane != 0) return;
+  if (S == 1) {  // the slice is the whole row
+    write_row_stats(p.stats, r, a);
+  } else {       // merged by the commit kernel
     p.ws.part_m[item] = a.m;
     p.ws.part_s[item] = a.s;
     p.ws.part_i[item] = a.idx;
-    last = atomic_add_acq_rel(p.ws.row_cnt + r, 1) == S - 1;
   }
-  last = __shfl_sync(kFull, last, 0);
-  if (!last) return;
-  RowAcc t = row_acc_empty();
-  for (int j = lane; j < S; j += 32) {
-    const int64_t pi = r * S + j;
-    t = row_acc_merge(t, RowAcc{__ldcg(p.ws.part_m + pi), __ldcg(p.ws.part_s + pi),
-                                __ldcg(p.ws.part_i + pi)});
-  }
-  t = row_acc_warp_reduce(t);
-  if (lane == 0) {
-    p.stats.row_max[r] = t.m;
-    p.stats.lse[r] = t.m + logf(t.s);
-    p.stats.conf[r] = 1.f / t.s;
-    p.stats.argmax[r] = t.idx;
-    p.ws.row_cnt[r] = 0;  // re-armed for the next launch on this workspace
+}
+
+// Merge the S slice partials of every row of sequence b that was read into its statistics.
+// Four threads per row, each folding every fourth slice (loads issued in batches of 16), then a
+// 4-lane shuffle merge; rows not read keep the -inf statistics the first kernel wrote.
+__device__ void merge_sequence(const CommitOnlyParams& p, int b) {
+  constexpr int kGroup = 4, kBatch = 16;
+  const int L = p.c.L, S = p.S;
+  const int q = threadIdx.x & (kGroup - 1);
+  const bool seq_read = p.eos_hit == nullptr || p.eos_hit[b] == 0;
+  for (int i0 = 0; i0 < L; i0 += kThreads / kGroup) {  // uniform trip count: shuffles below
+    const int i = i0 + static_cast<int>(threadIdx.x) / kGroup;
+    const int64_t r = static_cast<int64_t>(b) * L + i;
+    const bool read = i < L && seq_read && (p.masked == nullptr || p.masked[r]);
+    RowAcc t = row_acc_empty();
+    if (read) {
+      const int64_t base = r * S;
+      for (int j0 = q; j0 < S; j0 += kGroup * kBatch) {
+        float m[kBatch], sm[kBatch];
+        int ix[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int j = j0 + u * kGroup;
+          const bool ok = j < S;
+          m[u] = ok ? __ldcg(p.part_m + base + j) : -INFINITY;
+          sm[u] = ok ? __ldcg(p.part_s + base + j) : 0.f;
+          ix[u] = ok ? __ldcg(p.part_i + base + j) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) t = row_acc_merge(t, RowAcc{m[u], sm[u], ix[u]});
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < kGroup; o <<= 1) t = row_acc_merge(t, row_acc_shfl_xor(t, o));
+    if (read && q == 0) write_row_stats(p.stats, r, t);
   }
 }
 
 __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams p) {
   extern __shared__ __align__(1024) uint8_t dyn[];
   // launched after the statistics kernel as a programmatic dependent launch (or plainly):
-  // wait until every statistic and every read of the block state there is complete
+  // wait until every partial, statistic and read of the block state there is complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x;
   const int L = p.c.L;
   const int b = blockIdx.x;
+  if (p.S > 1) {
+    merge_sequence(p, b);
+    __syncthreads();  // this CTA's statistic writes are visible to its other threads
+  }
+  if (p.c.ca.mode == kStatsOnly) return;
   const EpiSmem sm = carve(dyn, L);
   const int64_t r0 = static_cast<int64_t>(b) * L;
   int any_masked = 0;
@@ -498,8 +531,8 @@ __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams 
   any_masked = __syncthreads_or(any_masked);
   const bool stopped = p.c.state.eos_hit[b] != 0 || !any_masked;
   for (int i = tid; i < L; i += kThreads) {
-    sm.val[i] = (sm.mask[i] && !stopped) ? p.stats.conf[r0 + i] : 0.f;
-    sm.am[i] = p.stats.argmax[r0 + i];
+    sm.val[i] = (sm.mask[i] && !stopped) ? __ldcg(p.stats.conf + r0 + i) : 0.f;
+    sm.am[i] = __ldcg(p.stats.argmax + r0 + i);
   }
   __syncthreads();
   commit_sequence(p.c, b, stopped, sm);
@@ -518,9 +551,8 @@ void choose_split(int V, int dtype, int* S_out, int* chunk_out) {
 int max_splits(int V) { return std::max(1, (V + 1023) / 1024); }
 
 size_t stats_ws_bytes(int B, int L, int V) {
-  const size_t R = static_cast<size_t>(B) * L;
-  const size_t parts = R * max_splits(V);
-  return kWsHeader + align_up(4 * R, 256) + 3 * align_up(4 * parts, 256);
+  const size_t parts = static_cast<size_t>(B) * L * max_splits(V);
+  return kWsHeader + 3 * align_up(4 * parts, 256);
 }
 
 StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
@@ -529,8 +561,6 @@ StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
   StatsWs w;
   w.status = reinterpret_cast<int32_t*>(p);
   p += kWsHeader;
-  w.row_cnt = reinterpret_cast<int32_t*>(p);
-  p += align_up(4 * static_cast<size_t>(B) * L, 256);
   w.part_m = reinterpret_cast<float*>(p);
   p += align_up(4 * parts, 256);
   w.part_s = reinterpret_cast<float*>(p);
@@ -572,11 +602,17 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
     stats_partials_kernel<DLLM_F32><<<grid1, kThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (ca.mode == kStatsOnly) return cudaSuccess;
-  // the commit kernel, one CTA per sequence, as a programmatic dependent launch
+  if (ca.mode == kStatsOnly && p.S == 1) return cudaSuccess;
+  // the merge (+ commit) kernel, one CTA per sequence, as a programmatic dependent launch
   CommitOnlyParams cp{};
   cp.stats = stats;
   cp.c = p.c;
+  cp.S = p.S;
+  cp.part_m = ws.part_m;
+  cp.part_s = ws.part_s;
+  cp.part_i = ws.part_i;
+  cp.masked = p.masked;
+  cp.eos_hit = p.eos_hit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.B);
   cfg.blockDim = dim3(kThreads);
@@ -599,6 +635,7 @@ cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,
   p.c.L = sh.L;
   p.c.state = state;
   p.c.ca = ca;
+  p.S = 1;  // statistics already complete: commit only
   commit_only_kernel<<<sh.B, kThreads, epi_smem_bytes(sh.L), stream>>>(p);
   return cudaGetLastError();
 }

@@ -251,9 +251,9 @@ dllm_status dllm_selftest_wait_timeout(void* ws, uint32_t limit_us, dllm_stream_
  *    DLLM_ERR_UNSUPPORTED (4 MiB: e.g. B*L up to 16384 rows at V = 126464).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *    that device current; make that first call before any stream capture.
- *  - Each call clears the array's status word and row counters on `stream`; nothing is
- *    allocated or freed.  All calls share the one array and it keeps the last call's contents, so calls
- *    that overlap on the GPU (different streams, or concurrent graphs) race: serialise them.
+ *  - Each call clears the array's status word on `stream`; nothing is allocated or freed.
+ *    All calls share the one array and it keeps the last call's contents, so calls that
+ *    overlap on the GPU (different streams, or concurrent graphs) race: serialise them.
  *  - dllm_get_status cannot be used on this scratch; a fault inside the kernel still surfaces
  *    as wrong results only, as for any call whose status word is never read.
  */
