@@ -15,41 +15,12 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mbarrier.cuh"
 
 namespace dllm {
 namespace {
 
 // ------------------------------------------------------------------ PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// 16-byte asynchronous global -> shared copy (LSU path; bypasses L1).
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
 
 // TMA box (0, y, slab) of a K-slab-blocked operand (rows y.. of one 64-wide K slab) into this
 // CTA's shared memory.  .cta_group::2: the completion may be signalled on an mbarrier in either
@@ -94,18 +65,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -171,42 +130,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
-
-// Bounded wait on an mbarrier phase.  The fast path is a plain try_wait spin; the clock and the
-// CTA's abort flag are consulted only every 1024 polls (reading them on every poll lengthened
-// each producer/consumer hand-off by microseconds).  On timeout: raise the CTA's abort flag and
-// record DLLM_ERR_TIMEOUT in the workspace status word; every other waiter then gives up too.
-template <bool kCluster = false>
-__device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                         int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
-  auto probe = [&]() {
-    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-  };
-  uint64_t t0 = 0;
-  for (uint32_t spins = 0;; ++spins) {
-    if (probe()) return true;
-    if ((spins & 1023u) == 1023u) {
-      if (*abort_flag) return false;
-      const uint64_t now = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > limit_ns) {
-        *abort_flag = 1;
-        set_status(status, DLLM_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// Short bounded wait used only while draining after an abort.
-__device__ void drain_bar(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < 100000000ull) {
-  }
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing ever arrives at;
