@@ -159,6 +159,47 @@ def rank_seed(base: int, rank: int) -> int:
 
 # ------------------------------------------------------------------ our arm: smooth_step
 
+# Translation units (with the headers they include) whose source a DRAM-traffic figure in
+# profiles/traffic.md was measured on; a figure counts only while that source is unchanged.
+_KERNEL_SOURCES = {
+    "smooth_gemm_kernel": ["smooth.cu", "mbarrier.cuh"],
+    "prob_rows_kernel": ["smooth.cu", "mbarrier.cuh"],
+    "stats_partials_kernel": ["stats_commit.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    csrc = os.path.join(root, "diffusion_decoding_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in _KERNEL_SOURCES[kernel] + ["common.cuh", "internal.h"]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    with open(os.path.join(root, "include", "dllm.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch from the ncu capture recorded in profiles/traffic.md
+    for this kernel and workload, or None when there is none or the kernel source changed."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash(kernel)
+    with open(path) as f:
+        for line in f:
+            cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload:
+                try:
+                    nbytes = float(cells[3])
+                except ValueError:
+                    continue
+                return nbytes if cells[2] == want else None
+    return None
+
+
 def algorithmic_bytes_stats(w, rows_read: int) -> int:
     """Logit bytes one stats launch must read (masked rows only) + state/stat writes."""
     es = 2 if w.dtype == "bf16" else 4
@@ -224,6 +265,20 @@ def run_smooth_step(args, rank, world, local):
     torch.cuda.synchronize(dev)
     Mv = int(M.item())
 
+    # the whole step (state reset + commit + smoothing + refresh) captured once into a CUDA
+    # graph and replayed: the kernels run back to back without host launch gaps
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step(logits)
+    stream.wait_stream(cap)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    assert int(M.item()) == Mv
+
     # per-kernel timing (events on the launching stream), then the whole-step timing
     t_stats, t_gemm, t_prob = [], [], []
     for _ in range(args.steps):
@@ -236,13 +291,13 @@ def run_smooth_step(args, rank, world, local):
 
     clocks = ClockSampler(local)
     clocks.start()
-    load_for(lambda: step(logits), 1.5, dev)  # same step, so the sampler sees it under load
+    load_for(graph.replay, 1.5, dev)  # same step, so the sampler sees it under load
     barrier(world)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step(logits)
+        graph.replay()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -253,7 +308,7 @@ def run_smooth_step(args, rank, world, local):
 
     # end to end through the public API with host buffers: H2D logits, step, D2H results
     lg_pin = torch.from_numpy(lg_host.view(np.int16)).pin_memory()
-    lg_dev = torch.empty(B, L, V, dtype=torch.int16, device=dev)
+    lg_dev = logits.view(torch.int16)  # the graph reads the logits from this buffer
     res_dev = [state.tokens, state.masked, state.n_commit, row_ids, M, out, idx, count]
     res_pin = [torch.empty_like(t, device="cpu").pin_memory() for t in res_dev]
     h2d = lg_pin.numel() * 2
@@ -261,7 +316,7 @@ def run_smooth_step(args, rank, world, local):
 
     def e2e_step():
         lg_dev.copy_(lg_pin, non_blocking=True)
-        step(lg_dev.view(torch.bfloat16))
+        graph.replay()
         for hp, dv in zip(res_pin, res_dev):
             hp.copy_(dv, non_blocking=True)
 
@@ -289,7 +344,7 @@ def run_smooth_step(args, rank, world, local):
     prob_gbs = prob_bytes / (prob_ms * 1e-3) / 1e9
     step_bytes = R * V * 2
     plan = dd.dllm_smooth_plan_info(shape, d)
-    launches_per_step = 1 + plan["launches"] + 1  # commit, smoothing kernels, refresh
+    launches_per_step = 2 + plan["launches"] + 1  # statistics + commit, smoothing, refresh
     res = {
         "metric": METRIC,
         "value": world * B * 1e3 / ms,
@@ -307,6 +362,7 @@ def run_smooth_step(args, rank, world, local):
                                "(softmax x E, d=2048) + KV refresh (prefix 1024, window 4)",
                    "B": B, "L_block": L, "V": V, "d": d, "M_smoothed": Mv, "gemm_plan": plan,
                    "l2": "inputs larger than L2 (259 MB logits + 518 MB table per step)",
+                   "launch": "whole step captured in one CUDA graph, replayed per step",
                    "parallelism": f"replicas x{world}"},
         "iters_per_s": 1e3 / ms,
         "logit_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
@@ -315,17 +371,21 @@ def run_smooth_step(args, rank, world, local):
                      "frac": gemm_tf / peaks["bf16_tflops_sustained"],
                      "peak_source": f"{peak_src} bf16 sustained",
                      "frac_of_burst": gemm_tf / peaks["bf16_tflops"],
-                     "traffic": None, "ms": gemm_ms,
+                     "traffic": measured_traffic("smooth_gemm_kernel", "smooth_step"),
+                     "traffic_unit": "DRAM bytes per launch", "ms": gemm_ms,
                      "algorithmic": f"2*M*V*d = {flops:.4g} FLOP per launch"},
         "roofline_stats": {"bound": "hbm", "kernel": "stats_partials_kernel + commit_only_kernel (one commit call)", "achieved": stats_gbs,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": stats_gbs / peaks["hbm_gbs"], "frac_of_8tbs": stats_gbs / 8000,
-                           "peak_source": f"{peak_src} HBM copy", "traffic": None,
+                           "peak_source": f"{peak_src} HBM copy",
+                           "traffic": measured_traffic("stats_partials_kernel", "smooth_step"),
+                           "traffic_unit": "DRAM bytes per launch (statistics kernel)",
                            "ms": stats_ms,
                            "algorithmic": f"{stats_bytes} logit bytes per launch"},
         "roofline_probs": {"bound": "hbm", "kernel": "prob_rows_kernel", "achieved": prob_gbs,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": prob_gbs / peaks["hbm_gbs"], "ms": prob_ms},
+                           "frac": prob_gbs / peaks["hbm_gbs"], "ms": prob_ms,
+                           "traffic": measured_traffic("prob_rows_kernel", "smooth_step")},
         "e2e": {"value": world * B * 1e3 / ms_e2e, "unit": "block-iters/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": launches_per_step * args.steps,
@@ -446,7 +506,7 @@ def run_loop(args, rank, world, local, key):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs1 / peaks["hbm_gbs"],
                      "peak_source": f"{peak_src} HBM copy", "traffic": None, "ms": ms1,
                      "algorithmic": f"{rows[0]} rows x V x {es} B"},
-        "gpu_launches": n_it * args.steps,
+        "gpu_launches": 2 * n_it * args.steps,  # statistics + commit per iteration
         "clocks": clk,
     }
 
