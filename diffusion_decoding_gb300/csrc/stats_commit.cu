@@ -471,39 +471,48 @@ __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams
   }
 }
 
-// Merge the S slice partials of every row of sequence b that was read into its statistics.
-// Four threads per row, each folding every fourth slice (loads issued in batches of 16), then a
-// 4-lane shuffle merge; rows not read keep the -inf statistics the first kernel wrote.
-__device__ void merge_sequence(const CommitOnlyParams& p, int b) {
+// Merge the S slice partials of every row of sequence b that was read into its statistics,
+// leaving (mask, confidence, argmax) of each position in shared memory for the commit.  Four
+// threads per row, each folding every fourth slice; the mask byte and the partials are loaded in
+// one round (partials of rows that turn out not to be read are loaded and ignored), then a
+// 4-lane shuffle merge.  Rows not read keep the -inf statistics the first kernel wrote.
+__device__ void merge_sequence(const CommitOnlyParams& p, int b, const uint8_t* mask_ptr,
+                               bool seq_read, const EpiSmem& sm) {
   constexpr int kGroup = 4, kBatch = 16;
   const int L = p.c.L, S = p.S;
   const int q = threadIdx.x & (kGroup - 1);
-  const bool seq_read = p.eos_hit == nullptr || p.eos_hit[b] == 0;
   for (int i0 = 0; i0 < L; i0 += kThreads / kGroup) {  // uniform trip count: shuffles below
     const int i = i0 + static_cast<int>(threadIdx.x) / kGroup;
-    const int64_t r = static_cast<int64_t>(b) * L + i;
-    const bool read = i < L && seq_read && (p.masked == nullptr || p.masked[r]);
+    const bool in = i < L;
+    const int64_t r = static_cast<int64_t>(b) * L + (in ? i : 0);
+    const uint8_t mk = in ? (mask_ptr == nullptr ? 1 : mask_ptr[r]) : 0;
+    const int64_t base = r * S;
     RowAcc t = row_acc_empty();
-    if (read) {
-      const int64_t base = r * S;
-      for (int j0 = q; j0 < S; j0 += kGroup * kBatch) {
-        float m[kBatch], sm[kBatch];
-        int ix[kBatch];
+    for (int j0 = q; j0 < S; j0 += kGroup * kBatch) {
+      float m[kBatch], sv[kBatch];
+      int ix[kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int j = j0 + u * kGroup;
-          const bool ok = j < S;
-          m[u] = ok ? __ldcg(p.part_m + base + j) : -INFINITY;
-          sm[u] = ok ? __ldcg(p.part_s + base + j) : 0.f;
-          ix[u] = ok ? __ldcg(p.part_i + base + j) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) t = row_acc_merge(t, RowAcc{m[u], sm[u], ix[u]});
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kGroup;
+        const bool ok = in && j < S;
+        m[u] = ok ? __ldcg(p.part_m + base + j) : -INFINITY;
+        sv[u] = ok ? __ldcg(p.part_s + base + j) : 0.f;
+        ix[u] = ok ? __ldcg(p.part_i + base + j) : -1;
       }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) t = row_acc_merge(t, RowAcc{m[u], sv[u], ix[u]});
     }
 #pragma unroll
     for (int o = 1; o < kGroup; o <<= 1) t = row_acc_merge(t, row_acc_shfl_xor(t, o));
-    if (read && q == 0) write_row_stats(p.stats, r, t);
+    if (in && q == 0) {
+      const bool read = seq_read && mk;
+      if (read) write_row_stats(p.stats, r, t);
+      if (sm.val != nullptr) {
+        sm.mask[i] = mk;
+        sm.val[i] = read ? 1.f / t.s : 0.f;
+        sm.am[i] = read ? t.idx : -1;
+      }
+    }
   }
 }
 
@@ -515,26 +524,31 @@ __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams 
   const int tid = threadIdx.x;
   const int L = p.c.L;
   const int b = blockIdx.x;
-  if (p.S > 1) {
-    merge_sequence(p, b);
-    __syncthreads();  // this CTA's statistic writes are visible to its other threads
-  }
-  if (p.c.ca.mode == kStatsOnly) return;
-  const EpiSmem sm = carve(dyn, L);
+  const bool commit = p.c.ca.mode != kStatsOnly;
   const int64_t r0 = static_cast<int64_t>(b) * L;
+  const int32_t* eos_ptr = commit ? p.c.state.eos_hit : p.eos_hit;
+  const uint8_t* mask_ptr = commit ? p.c.state.masked : p.masked;
+  const bool seq_read = eos_ptr == nullptr || eos_ptr[b] == 0;
+  EpiSmem sm = carve(dyn, L);
+  if (!commit) sm.val = nullptr;  // statistics only: nothing to stage
+  if (p.S > 1) {
+    merge_sequence(p, b, mask_ptr, seq_read, sm);
+  } else if (commit) {  // statistics already complete: mask and statistics in one round of loads
+    for (int i = tid; i < L; i += kThreads) {
+      const uint8_t mk = mask_ptr[r0 + i];
+      const float cf = __ldcg(p.stats.conf + r0 + i);
+      const int am = __ldcg(p.stats.argmax + r0 + i);
+      sm.mask[i] = mk;
+      sm.val[i] = (mk && seq_read) ? cf : 0.f;
+      sm.am[i] = am;
+    }
+  }
+  if (!commit) return;
   int any_masked = 0;
-  for (int i = tid; i < L; i += kThreads) {
-    const uint8_t m = p.c.state.masked[r0 + i];
-    sm.mask[i] = m;
-    any_masked |= m;
-  }
-  any_masked = __syncthreads_or(any_masked);
-  const bool stopped = p.c.state.eos_hit[b] != 0 || !any_masked;
-  for (int i = tid; i < L; i += kThreads) {
-    sm.val[i] = (sm.mask[i] && !stopped) ? __ldcg(p.stats.conf + r0 + i) : 0.f;
-    sm.am[i] = __ldcg(p.stats.argmax + r0 + i);
-  }
   __syncthreads();
+  for (int i = tid; i < L; i += kThreads) any_masked |= sm.mask[i];
+  any_masked = __syncthreads_or(any_masked);
+  const bool stopped = !seq_read || !any_masked;
   commit_sequence(p.c, b, stopped, sm);
 }
 
