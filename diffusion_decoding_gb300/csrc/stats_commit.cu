@@ -24,7 +24,6 @@ namespace dllm {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxWarps = kThreads / 32;
 
 struct CommitCtx {
   int B, L;
@@ -36,6 +35,7 @@ struct FusedParams {
   const char* logits;
   int64_t row_stride_bytes;
   int V, S, chunk;
+  int pdl_from;            // CTAs from this index on let the dependent commit grid launch
   const uint8_t* masked;   // rows to read (state.masked when committing)
   const int32_t* eos_hit;  // null in statistics-only mode
   dllm_stats stats;
@@ -207,9 +207,11 @@ __device__ __forceinline__ RowAcc warp_reduce_slice(const char* row, int64_t e0,
 
 // ------------------------------------------------------------------ block helpers
 
+constexpr int kBlockWarpsMax = 32;  // the block helpers below serve blocks of up to 1024 threads
+
 // In-place inclusive max-scan of a[0..n) (values >= -1) with warp shuffles; ends synchronised.
 __device__ void block_max_scan(int* a, int n) {
-  __shared__ int warp_tot[kMaxWarps];
+  __shared__ int warp_tot[kBlockWarpsMax];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = blockDim.x;
   const int ipt = (n + nt - 1) / nt;
@@ -237,8 +239,8 @@ __device__ void block_max_scan(int* a, int n) {
 
 // Masked position of largest value, lowest index on ties (-1 if nothing is masked).
 __device__ int block_masked_argmax(const float* val, const uint8_t* mask, int L) {
-  __shared__ float wv[kMaxWarps];
-  __shared__ int wi[kMaxWarps];
+  __shared__ float wv[kBlockWarpsMax];
+  __shared__ int wi[kBlockWarpsMax];
   __shared__ int result;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = blockDim.x, nw = nt >> 5;
@@ -438,8 +440,10 @@ __device__ __forceinline__ void write_row_stats(const dllm_stats& st, int64_t r,
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams p) {
-  // let the commit kernel's CTAs become resident while this grid drains
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // let the commit kernel's CTAs become resident while this grid's last waves run (earlier
+  // CTAs count as triggered when they exit, so its CTAs do not hold SMs for the whole pass)
+  if (static_cast<int>(blockIdx.x) >= p.pdl_from)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp;
   const int S = p.S, L = p.c.L;
@@ -471,41 +475,70 @@ __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams
   }
 }
 
+constexpr int kCommitThreads = 512;
+
 // Merge the S slice partials of every row of sequence b that was read into its statistics,
-// leaving (mask, confidence, argmax) of each position in shared memory for the commit.  Four
-// threads per row, each folding every fourth slice; the mask byte and the partials are loaded in
-// one round (partials of rows that turn out not to be read are loaded and ignored), then a
-// 4-lane shuffle merge.  Rows not read keep the -inf statistics the first kernel wrote.
+// leaving (mask, confidence, argmax) of each position in shared memory for the commit.  Eight
+// threads per row; each loads its share of the row's partials together with the row's mask
+// byte (partials of rows that turn out not to be read are loaded and ignored).  The row maximum
+// M is taken first (max over the partial maxima, then over the 8 lanes); then every partial
+// sum is rescaled once, s_j * exp(m_j - M), independently of the others, and the lowest index
+// among the partials whose maximum equals M is the argmax.  Rows not read keep the -inf
+// statistics the first kernel wrote.
 __device__ void merge_sequence(const CommitOnlyParams& p, int b, const uint8_t* mask_ptr,
                                bool seq_read, const EpiSmem& sm) {
-  constexpr int kGroup = 4, kBatch = 16;
+  constexpr int kGroup = 8, kBatch = 8;
   const int L = p.c.L, S = p.S;
   const int q = threadIdx.x & (kGroup - 1);
-  for (int i0 = 0; i0 < L; i0 += kThreads / kGroup) {  // uniform trip count: shuffles below
+  for (int i0 = 0; i0 < L; i0 += kCommitThreads / kGroup) {  // uniform trip count: shuffles
     const int i = i0 + static_cast<int>(threadIdx.x) / kGroup;
     const bool in = i < L;
     const int64_t r = static_cast<int64_t>(b) * L + (in ? i : 0);
     const uint8_t mk = in ? (mask_ptr == nullptr ? 1 : mask_ptr[r]) : 0;
     const int64_t base = r * S;
-    RowAcc t = row_acc_empty();
-    for (int j0 = q; j0 < S; j0 += kGroup * kBatch) {
+    float M = -INFINITY, sum = 0.f;
+    int idx = INT_MAX;
+    // trip count uniform across the 8 lanes (the batch maximum is shuffled among them)
+    for (int j0 = 0; j0 < S; j0 += kGroup * kBatch) {  // one pass whenever S <= 64
       float m[kBatch], sv[kBatch];
       int ix[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int j = j0 + u * kGroup;
+        const int j = j0 + q + u * kGroup;
         const bool ok = in && j < S;
         m[u] = ok ? __ldcg(p.part_m + base + j) : -INFINITY;
         sv[u] = ok ? __ldcg(p.part_s + base + j) : 0.f;
         ix[u] = ok ? __ldcg(p.part_i + base + j) : -1;
       }
+      float bm = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) t = row_acc_merge(t, RowAcc{m[u], sv[u], ix[u]});
+      for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, m[u]);
+#pragma unroll
+      for (int o = 1; o < kGroup; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, o));
+      // fold this batch into the running (M, sum, idx)
+      const float nM = fmaxf(M, bm);
+      if (nM != -INFINITY) {
+        if (nM > M) {  // the maximum rose: rescale the running sum; earlier indices lose
+          sum = (M == -INFINITY) ? 0.f : sum * ex2((M - nM) * kLog2e);
+          idx = INT_MAX;
+        }
+        const float nb = nM * kLog2e;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (m[u] != -INFINITY) sum = fmaf(sv[u], ex2(fmaf(m[u], kLog2e, -nb)), sum);
+          if (m[u] == nM && ix[u] >= 0) idx = min(idx, ix[u]);
+        }
+        M = nM;
+      }
     }
 #pragma unroll
-    for (int o = 1; o < kGroup; o <<= 1) t = row_acc_merge(t, row_acc_shfl_xor(t, o));
+    for (int o = 1; o < kGroup; o <<= 1) {
+      sum += __shfl_xor_sync(kFull, sum, o);
+      idx = min(idx, __shfl_xor_sync(kFull, idx, o));
+    }
     if (in && q == 0) {
       const bool read = seq_read && mk;
+      const RowAcc t{M, sum, idx == INT_MAX ? -1 : idx};
       if (read) write_row_stats(p.stats, r, t);
       if (sm.val != nullptr) {
         sm.mask[i] = mk;
@@ -516,7 +549,7 @@ __device__ void merge_sequence(const CommitOnlyParams& p, int b, const uint8_t* 
   }
 }
 
-__global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams p) {
+__global__ void __launch_bounds__(kCommitThreads) commit_only_kernel(CommitOnlyParams p) {
   extern __shared__ __align__(1024) uint8_t dyn[];
   // launched after the statistics kernel as a programmatic dependent launch (or plainly):
   // wait until every partial, statistic and read of the block state there is complete
@@ -534,7 +567,7 @@ __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams 
   if (p.S > 1) {
     merge_sequence(p, b, mask_ptr, seq_read, sm);
   } else if (commit) {  // statistics already complete: mask and statistics in one round of loads
-    for (int i = tid; i < L; i += kThreads) {
+    for (int i = tid; i < L; i += kCommitThreads) {
       const uint8_t mk = mask_ptr[r0 + i];
       const float cf = __ldcg(p.stats.conf + r0 + i);
       const int am = __ldcg(p.stats.argmax + r0 + i);
@@ -546,7 +579,7 @@ __global__ void __launch_bounds__(kThreads) commit_only_kernel(CommitOnlyParams 
   if (!commit) return;
   int any_masked = 0;
   __syncthreads();
-  for (int i = tid; i < L; i += kThreads) any_masked |= sm.mask[i];
+  for (int i = tid; i < L; i += kCommitThreads) any_masked |= sm.mask[i];
   any_masked = __syncthreads_or(any_masked);
   const bool stopped = !seq_read || !any_masked;
   commit_sequence(p.c, b, stopped, sm);
@@ -607,9 +640,9 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
     p.masked = state->masked;
     p.eos_hit = state->eos_hit;
   }
-  (void)sm_count;
   const int64_t items = static_cast<int64_t>(R) * p.S;
   const dim3 grid1(static_cast<unsigned>((items + kThreads / 32 - 1) / (kThreads / 32)));
+  p.pdl_from = std::max(0, static_cast<int>(grid1.x) - 2 * 4 * std::max(1, sm_count));
   if (sh.dtype == DLLM_BF16)
     stats_partials_kernel<DLLM_BF16><<<grid1, kThreads, 0, stream>>>(p);
   else
@@ -629,7 +662,7 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   cp.eos_hit = p.eos_hit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.B);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kCommitThreads);
   cfg.dynamicSmemBytes = epi_smem_bytes(sh.L);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -650,7 +683,7 @@ cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,
   p.c.state = state;
   p.c.ca = ca;
   p.S = 1;  // statistics already complete: commit only
-  commit_only_kernel<<<sh.B, kThreads, epi_smem_bytes(sh.L), stream>>>(p);
+  commit_only_kernel<<<sh.B, kCommitThreads, epi_smem_bytes(sh.L), stream>>>(p);
   return cudaGetLastError();
 }
 
