@@ -30,9 +30,7 @@ struct CommitArgs {
 // Stats/commit workspace layout.
 struct StatsWs {
   int32_t* status;
-  float* part_m;      // [R * S_max]
-  float* part_s;
-  int32_t* part_i;
+  uint4* part;        // [R * S_max] one {max, sum, argmax, 0} record (16 bytes) per slice
 };
 
 int max_splits(int V);

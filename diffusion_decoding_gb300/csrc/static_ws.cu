@@ -21,8 +21,8 @@
 
 namespace {
 
-// 4 MiB: room for the partials of B*L*ceil(V/8192) <= ~349,000 row slices (for example B*L =
-// 1024 rows at V up to ~2.8 million, or B*L = 16384 rows at V = 126464).
+// 4 MiB: room for ~262,000 slice records of 16 bytes, B*L*ceil(V/1024) of them (for example
+// B*L = 1024 rows at V up to ~262,000, or B*L = 2048 rows at V = 126464).
 constexpr size_t kStaticWsBytes = DLLM_STATIC_WORKSPACE_BYTES;
 constexpr int kMaxDevices = 64;
 

@@ -47,9 +47,7 @@ struct CommitOnlyParams {
   dllm_stats stats;
   CommitCtx c;
   int S;                  // slices per row (1: the statistics are complete, nothing to merge)
-  const float* part_m;    // [R * S] slice partials
-  const float* part_s;
-  const int32_t* part_i;
+  const uint4* part;      // [R * S] slice partials {max, sum, argmax, 0}
   const uint8_t* masked;  // rows that were read (null: all rows; statistics-only mode)
   const int32_t* eos_hit; // null in statistics-only mode
 };
@@ -469,9 +467,8 @@ __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams
   if (S == 1) {  // the slice is the whole row
     write_row_stats(p.stats, r, a);
   } else {       // merged by the commit kernel
-    p.ws.part_m[item] = a.m;
-    p.ws.part_s[item] = a.s;
-    p.ws.part_i[item] = a.idx;
+    p.ws.part[item] = make_uint4(__float_as_uint(a.m), __float_as_uint(a.s),
+                                 static_cast<uint32_t>(a.idx), 0u);
   }
 }
 
@@ -506,9 +503,11 @@ __device__ void merge_sequence(const CommitOnlyParams& p, int b, const uint8_t* 
       for (int u = 0; u < kBatch; ++u) {
         const int j = j0 + q + u * kGroup;
         const bool ok = in && j < S;
-        m[u] = ok ? __ldcg(p.part_m + base + j) : -INFINITY;
-        sv[u] = ok ? __ldcg(p.part_s + base + j) : 0.f;
-        ix[u] = ok ? __ldcg(p.part_i + base + j) : -1;
+        const uint4 v = ok ? __ldcg(p.part + base + j)
+                           : make_uint4(__float_as_uint(-INFINITY), 0u, 0xFFFFFFFFu, 0u);
+        m[u] = __uint_as_float(v.x);
+        sv[u] = __uint_as_float(v.y);
+        ix[u] = static_cast<int>(v.z);
       }
       float bm = -INFINITY;
 #pragma unroll
@@ -599,7 +598,7 @@ int max_splits(int V) { return std::max(1, (V + 1023) / 1024); }
 
 size_t stats_ws_bytes(int B, int L, int V) {
   const size_t parts = static_cast<size_t>(B) * L * max_splits(V);
-  return kWsHeader + 3 * align_up(4 * parts, 256);
+  return kWsHeader + align_up(16 * parts, 256);
 }
 
 StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
@@ -608,11 +607,8 @@ StatsWs stats_ws_layout(void* ws, int B, int L, int V) {
   StatsWs w;
   w.status = reinterpret_cast<int32_t*>(p);
   p += kWsHeader;
-  w.part_m = reinterpret_cast<float*>(p);
-  p += align_up(4 * parts, 256);
-  w.part_s = reinterpret_cast<float*>(p);
-  p += align_up(4 * parts, 256);
-  w.part_i = reinterpret_cast<int32_t*>(p);
+  w.part = reinterpret_cast<uint4*>(p);
+  (void)parts;
   return w;
 }
 
@@ -655,9 +651,7 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   cp.stats = stats;
   cp.c = p.c;
   cp.S = p.S;
-  cp.part_m = ws.part_m;
-  cp.part_s = ws.part_s;
-  cp.part_i = ws.part_i;
+  cp.part = ws.part;
   cp.masked = p.masked;
   cp.eos_hit = p.eos_hit;
   cudaLaunchConfig_t cfg = {};

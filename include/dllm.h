@@ -248,7 +248,7 @@ dllm_status dllm_selftest_wait_timeout(void* ws, uint32_t limit_us, dllm_stream_
  * DLLM_STATIC_WORKSPACE_BYTES in device memory, part of the library image: every GPU that loads
  * the library holds it until the process exits.
  *  - Shapes whose dllm_workspace_bytes exceeds DLLM_STATIC_WORKSPACE_BYTES are rejected with
- *    DLLM_ERR_UNSUPPORTED (4 MiB: e.g. B*L up to 16384 rows at V = 126464).
+ *    DLLM_ERR_UNSUPPORTED (4 MiB: e.g. B*L up to 2048 rows at V = 126464).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *    that device current; make that first call before any stream capture.
  *  - Each call clears the array's status word on `stream`; nothing is allocated or freed.
