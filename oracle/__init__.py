@@ -51,10 +51,11 @@ def _load():
         _lib.orc_prob_row_bf16.argtypes = [vp, i32, i64, i64, i64, dbl, vp]
         _lib.orc_round_to_bf16.argtypes = [vp, i64, vp]
         _lib.orc_kv_refresh.argtypes = [i32, i32, vp, i32, i32, vp, vp, vp]
+        _lib.orc_merge_shard_stats.argtypes = [i32, i64, vp, vp, vp, vp, vp, vp, vp, vp]
         for name in ("orc_stats", "orc_active_rows", "orc_commit_threshold",
                      "orc_commit_hierarchical", "orc_commit_credit", "orc_smooth_rows",
                      "orc_smooth_embed", "orc_prob_row_bf16", "orc_round_to_bf16",
-                     "orc_kv_refresh"):
+                     "orc_kv_refresh", "orc_merge_shard_stats"):
             getattr(_lib, name).restype = ctypes.c_int
     return _lib
 
@@ -217,3 +218,19 @@ def kv_refresh(committed_now: np.ndarray, prefix_len: int, window: int):
                                 int(prefix_len), int(window), _p(refresh), _p(idx), _p(count))
     _check(rc, "kv_refresh")
     return refresh, idx, count
+
+
+def merge_shard_stats(shards: list, offsets) -> Stats:
+    """Merge per-shard Stats (each over its own vocabulary columns, local argmax) of the same R
+    rows; offsets[k] = first vocabulary id of shard k."""
+    n = len(shards)
+    R = shards[0].row_max.size
+    rm = np.ascontiguousarray(np.stack([s.row_max for s in shards]), np.float64)
+    ls = np.ascontiguousarray(np.stack([s.lse for s in shards]), np.float64)
+    am = np.ascontiguousarray(np.stack([s.argmax for s in shards]), np.int32)
+    off = np.ascontiguousarray(offsets, np.int64)
+    out = Stats(R)
+    rc = _load().orc_merge_shard_stats(n, R, _p(rm), _p(ls), _p(am), _p(off), _p(out.row_max),
+                                       _p(out.lse), _p(out.conf), _p(out.argmax))
+    _check(rc, "merge_shard_stats")
+    return out

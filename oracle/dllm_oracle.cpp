@@ -346,6 +346,49 @@ int orc_round_to_bf16(const double* x, int64_t n, double* y) {
   return 0;
 }
 
+// Statistics of rows whose vocabulary is split into n contiguous shards, from each shard's own
+// statistics (dInfer explainer, system optimisations: tensor parallelism splits the output layer,
+// so each GPU holds the logits of one vocabulary range).  Shard k covers ids
+// [offset[k], offset[k] + V_k) and reports, per row r, m_k = row_max[k*R + r],
+// lse_k = lse[k*R + r] and its local argmax a_k = argmax[k*R + r] (orc_stats of its columns).
+// Each shard's sum is s_k = exp(lse_k - m_k) against its own maximum, so over the whole row
+//   m = max_k m_k,   s = sum_k s_k exp(m_k - m) = sum_k exp(lse_k - m),
+//   lse = m + ln s,  conf = 1/s,  argmax = lowest offset[k] + a_k over the shards with m_k = m.
+// Shards reporting m_k = -inf (row not read) contribute nothing; a row no shard read reports
+// -inf, -inf, 0, -1.
+int orc_merge_shard_stats(int n, int64_t R, const double* row_max, const double* lse,
+                          const int32_t* argmax, const int64_t* offset, double* out_max,
+                          double* out_lse, double* out_conf, int32_t* out_argmax) {
+  if (n < 1 || R < 0) return 1;
+  for (int64_t r = 0; r < R; ++r) {
+    double m = kNegInf;
+    for (int k = 0; k < n; ++k) m = std::fmax(m, row_max[k * R + r]);
+    if (m == kNegInf) {
+      out_max[r] = kNegInf;
+      out_lse[r] = kNegInf;
+      out_conf[r] = 0.0;
+      out_argmax[r] = -1;
+      continue;
+    }
+    double s = 0.0;
+    int64_t am = -1;
+    for (int k = 0; k < n; ++k) {
+      const double mk = row_max[k * R + r];
+      if (mk == kNegInf) continue;
+      s += std::exp(lse[k * R + r] - m);
+      if (mk == m) {
+        const int64_t g = offset[k] + argmax[k * R + r];
+        if (am < 0 || g < am) am = g;
+      }
+    }
+    out_max[r] = m;
+    out_lse[r] = m + std::log(s);
+    out_conf[r] = 1.0 / s;
+    out_argmax[r] = static_cast<int32_t>(am);
+  }
+  return 0;
+}
+
 // Neighbourhood KV refresh (dInfer explainer, KV-cache manager: when a region changes, its cache
 // entries and those of its neighbours are recomputed).  Cache row = [prefix 0..P)[block P..P+L);
 // refresh[j] = 1 iff a position i committed in this step has |j - (P + i)| <= window.
