@@ -45,6 +45,10 @@ class dllm_stats(ctypes.Structure):
     _fields_ = [("row_max", _c_vp), ("lse", _c_vp), ("conf", _c_vp), ("argmax", _c_vp)]
 
 
+class dllm_shard_stats(ctypes.Structure):
+    _fields_ = [("stats", dllm_stats), ("vocab_offset", _c_i64)]
+
+
 _SIGS = {
     "dllm_last_error": (ctypes.c_char_p, []),
     "dllm_workspace_bytes": (_c_sz, [ctypes.POINTER(dllm_shape)]),
@@ -77,6 +81,8 @@ _SIGS = {
     "dllm_kv_refresh_mask": (_c_i32, [ctypes.POINTER(dllm_block_state), _c_i32, _c_i32, _c_i32,
                                       _c_i32, _c_vp, _c_vp, _c_vp, _c_vp]),
     "dllm_get_status": (_c_i32, [_c_vp, _c_vp, ctypes.POINTER(_c_i32)]),
+    "dllm_merge_shard_stats": (_c_i32, [ctypes.POINTER(dllm_shard_stats), _c_i32, _c_i64,
+                                        ctypes.POINTER(dllm_stats), _c_vp]),
     "dllm_selftest_wait_timeout": (_c_i32, [_c_vp, ctypes.c_uint32, _c_vp]),
     "dllm_commit_threshold_static": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape),
                                               ctypes.POINTER(dllm_stats),
@@ -298,6 +304,17 @@ def dllm_commit_threshold_static(logits, shape, stats: StatsBuffers, state: Bloc
 def dllm_selftest_wait_timeout(ws, limit_us: int, stream=None) -> None:
     _check(lib().dllm_selftest_wait_timeout(_ptr(ws), limit_us, _stream(stream)),
            "dllm_selftest_wait_timeout")
+
+
+def dllm_merge_shard_stats(shards, rows: int, out: StatsBuffers, stream=None) -> None:
+    """shards: list of (statistics of one vocabulary shard, its first vocabulary id); each
+    statistics object has row_max, lse, conf (float32) and argmax (int32) device tensors."""
+    arr = (dllm_shard_stats * len(shards))(*[
+        dllm_shard_stats(dllm_stats(_ptr(st.row_max), _ptr(st.lse), _ptr(st.conf),
+                                    _ptr(st.argmax)), int(off))
+        for st, off in shards])
+    _check(lib().dllm_merge_shard_stats(arr, len(shards), int(rows), ctypes.byref(out.c()),
+                                        _stream(stream)), "dllm_merge_shard_stats")
 
 
 def dllm_get_status(ws, stream=None) -> int:

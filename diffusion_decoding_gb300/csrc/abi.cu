@@ -324,6 +324,29 @@ dllm_status dllm_selftest_wait_timeout(void* ws, uint32_t limit_us, dllm_stream_
   return ok();
 }
 
+dllm_status dllm_merge_shard_stats(const dllm_shard_stats* shards, int32_t n, int64_t rows,
+                                   const dllm_stats* out, dllm_stream_t stream) {
+  if (!shards) return fail(DLLM_ERR_INVALID_ARG, "shards is null");
+  if (n < 1 || n > DLLM_MAX_SHARDS)
+    return fail(DLLM_ERR_INVALID_ARG, "n=%d must be in [1, %d]", n, DLLM_MAX_SHARDS);
+  if (rows < 0 || rows > (int64_t{1} << 31))
+    return fail(DLLM_ERR_INVALID_ARG, "rows=%lld out of range", static_cast<long long>(rows));
+  DLLM_TRY(check_stats(out));
+  for (int k = 0; k < n; ++k) {
+    DLLM_TRY(check_stats(&shards[k].stats));
+    if (shards[k].vocab_offset < 0 || shards[k].vocab_offset >= (int64_t{1} << 31))
+      return fail(DLLM_ERR_INVALID_ARG, "shard %d: vocab_offset out of range", k);
+    const dllm_stats& a = shards[k].stats;
+    if (a.row_max == out->row_max || a.lse == out->lse || a.conf == out->conf ||
+        a.argmax == out->argmax)
+      return fail(DLLM_ERR_INVALID_ARG, "shard %d aliases the output", k);
+  }
+  cudaError_t e = dllm::launch_merge_shard_stats(shards, n, rows, *out,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_merge_shard_stats");
+  return ok();
+}
+
 dllm_status dllm_get_status(void* ws, dllm_stream_t stream, int32_t* out_host) {
   DLLM_TRY(check_ws(ws));
   if (!out_host) return fail(DLLM_ERR_INVALID_ARG, "out_host is null");

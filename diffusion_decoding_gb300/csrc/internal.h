@@ -83,6 +83,9 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& plan, const uint16_t* P, const 
                                int ldt, float* out, const int32_t* M, void* ws,
                                cudaStream_t stream, const char** why);
 
+cudaError_t launch_merge_shard_stats(const dllm_shard_stats* shards, int n, int64_t rows,
+                                     const dllm_stats& out, cudaStream_t stream);
+
 cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns,
                                          cudaStream_t stream);
 

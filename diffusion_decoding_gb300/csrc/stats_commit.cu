@@ -584,6 +584,41 @@ __global__ void __launch_bounds__(kCommitThreads) commit_only_kernel(CommitOnlyP
   commit_sequence(p.c, b, stopped, sm);
 }
 
+// Vocabulary-sharded statistics: one thread per row folds the n shards' (m, lse, argmax).
+struct ShardParams {
+  dllm_shard_stats sh[DLLM_MAX_SHARDS];
+  int n;
+  int64_t rows;
+  dllm_stats out;
+};
+
+__global__ void __launch_bounds__(256) merge_shards_kernel(const __grid_constant__ ShardParams p) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= p.rows) return;
+  float m = -INFINITY;
+  for (int k = 0; k < p.n; ++k) m = fmaxf(m, p.sh[k].stats.row_max[r]);
+  if (m == -INFINITY) {
+    p.out.row_max[r] = -INFINITY;
+    p.out.lse[r] = -INFINITY;
+    p.out.conf[r] = 0.f;
+    p.out.argmax[r] = -1;
+    return;
+  }
+  float s = 0.f;
+  int64_t am = INT64_MAX;
+  const float mb = m * kLog2e;
+  for (int k = 0; k < p.n; ++k) {
+    const float mk = p.sh[k].stats.row_max[r];
+    if (mk == -INFINITY) continue;
+    s += ex2(fmaf(p.sh[k].stats.lse[r], kLog2e, -mb));
+    if (mk == m) am = min(am, p.sh[k].vocab_offset + p.sh[k].stats.argmax[r]);
+  }
+  p.out.row_max[r] = m;
+  p.out.lse[r] = m + logf(s);
+  p.out.conf[r] = 1.f / s;
+  p.out.argmax[r] = static_cast<int32_t>(am);
+}
+
 // One 4 KB warp slice per item.
 void choose_split(int V, int dtype, int* S_out, int* chunk_out) {
   const int chunk = dtype == DLLM_BF16 ? slice_elems<DLLM_BF16>() : slice_elems<DLLM_F32>();
@@ -665,6 +700,18 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, commit_only_kernel, cp);
+}
+
+cudaError_t launch_merge_shard_stats(const dllm_shard_stats* shards, int n, int64_t rows,
+                                     const dllm_stats& out, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  ShardParams p{};
+  for (int k = 0; k < n; ++k) p.sh[k] = shards[k];
+  p.n = n;
+  p.rows = rows;
+  p.out = out;
+  merge_shards_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,

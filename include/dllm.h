@@ -219,6 +219,27 @@ dllm_status dllm_smooth_gemm(const dllm_shape* shape, const uint16_t* Et, int32_
                              const int32_t* M, void* ws, size_t ws_bytes, dllm_stream_t stream);
 
 /*
+ * Statistics of rows whose vocabulary is split over n tensor-parallel shards (dInfer explainer,
+ * system optimisations: tensor parallelism splits the output layer, so each GPU holds the logits
+ * of one contiguous vocabulary range).  Shard k covers ids [vocab_offset, vocab_offset + V_k)
+ * and its `stats` are dllm_decode_stats of those columns (local argmax).  Per row:
+ *   row_max = max_k m_k;  s = sum_k exp(lse_k - row_max);  lse = row_max + ln s;  conf = 1/s;
+ *   argmax = lowest vocab_offset_k + argmax_k over the shards with m_k = row_max.
+ * A row that no shard read (all m_k = -inf) gets -inf, -inf, 0, -1.  Exchanging the shards'
+ * statistics (R x 16 bytes each, an all-gather) is the caller's: `shards` is a host array of n
+ * descriptors whose arrays are device memory on this GPU (this rank's own, or received).
+ * n in [1, DLLM_MAX_SHARDS]; rows >= 0; out may not alias a shard's arrays.  Asynchronous on
+ * `stream`; nothing is allocated.
+ */
+#define DLLM_MAX_SHARDS 64
+typedef struct {
+  dllm_stats stats;
+  int64_t vocab_offset;
+} dllm_shard_stats;
+dllm_status dllm_merge_shard_stats(const dllm_shard_stats* shards, int32_t n, int64_t rows,
+                                   const dllm_stats* out, dllm_stream_t stream);
+
+/*
  * Neighbourhood KV refresh (dInfer explainer, KV-cache manager: when a region of the sequence
  * changes, its cache entries and those of its neighbours are recomputed).  The cache row of
  * sequence b is [prefix 0..prefix_len) followed by the block, T = prefix_len + L entries:
