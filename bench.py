@@ -422,6 +422,108 @@ def run_smooth_step(args, rank, world, local):
     return res
 
 
+# ------------------------------------------------------------------ our arm: sharded vocabulary
+
+def run_tp_shards(args, rank, world, local, n_shards=8):
+    """One credit-decoding step (B=32, L=32, V=126464) with the vocabulary split over n_shards
+    tensor-parallel shards, all simulated on this GPU: each shard's statistics, the merge of the
+    shards' statistics, and the commit from the merged statistics, replayed as one CUDA graph.
+    (On n GPUs each rank would reduce only its own shard and all-gather R x 16 bytes.)"""
+    import diffusion_decoding_gb300 as dd
+    from diffusion_decoding_gb300.tp import vocab_range
+
+    w = WORKLOADS["credit_loop"]
+    dev = torch.device("cuda", local)
+    seed = rank_seed(SEEDS["credit_loop"], rank)
+    R = w.B * w.L
+    lg = synth.logits(w, seed, 0).reshape(R, w.V)
+    shards, stats_k, ws_k, shapes = [], [], [], []
+    for k in range(n_shards):
+        first, cnt = vocab_range(w.V, n_shards, k)
+        stride = -(-cnt // 8) * 8
+        buf = np.zeros((R, stride), np.uint16)
+        buf[:, :cnt] = lg[:, first:first + cnt]
+        shards.append(torch.from_numpy(buf.view(np.int16)).to(dev).view(torch.bfloat16))
+        shapes.append(dd.make_shape(1, R, cnt, dd.DLLM_BF16, row_stride=stride))
+        stats_k.append(dd.StatsBuffers(R, device=dev))
+        ws_k.append(dd.workspace(dd.dllm_workspace_bytes(shapes[-1]), dev))
+    offsets = [vocab_range(w.V, n_shards, k)[0] for k in range(n_shards)]
+    shape = dd.make_shape(w.B, w.L, w.V, dd.DLLM_BF16)
+    state = dd.BlockState(w.B, w.L, w.K, device=dev)
+    merged = dd.StatsBuffers(R, device=dev)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape), dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = {}
+
+    def step(timed=False):
+        state.reset()
+        for k in range(n_shards):
+            dd.dllm_decode_stats(shards[k], shapes[k], state.masked, stats_k[k], ws_k[k])
+        if timed:
+            ev["m0"].record(stream)
+        dd.dllm_merge_shard_stats(list(zip(stats_k, offsets)), R, merged)
+        if timed:
+            ev["m1"].record(stream)
+        dd.dllm_commit_credit(None, shape, merged, state, w.K, w.decay, w.boost, w.tau,
+                              w.eos_id, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t_merge = []
+    for _ in range(args.steps):
+        ev.update({k: torch.cuda.Event(enable_timing=True) for k in ("m0", "m1")})
+        step(timed=True)
+        torch.cuda.synchronize(dev)
+        t_merge.append(ev["m0"].elapsed_time(ev["m1"]))
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    stream.wait_stream(cap)
+    for _ in range(args.warmup):
+        graph.replay()
+    clocks = ClockSampler(local)
+    clocks.start()
+    load_for(graph.replay, 1.5, dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    peaks, peak_src = load_peaks()
+    step_bytes = R * w.V * 2
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": world * w.B * 1e3 / ms, "unit": "block-iters/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded planted-peak logits)",
+        "config": {"workload": f"tp{n_shards}_credit_step: vocabulary split over {n_shards} "
+                               "simulated tensor-parallel shards on one GPU, B=32 L=32 "
+                               "V=126464 bf16, credit commit from the merged statistics",
+                   "launch": "whole step captured in one CUDA graph, replayed per step",
+                   "parallelism": f"replicas x{world}"},
+        "iters_per_s": 1e3 / ms,
+        "roofline": {"bound": "hbm", "kernel": f"{n_shards} x statistics + merge + commit",
+                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+                     "traffic": None, "ms": ms,
+                     "algorithmic": f"{step_bytes} logit bytes per step"},
+        "merge_kernel_us": 1e3 * statistics.mean(t_merge),
+        "gpu_launches": (2 * n_shards + 2) * args.steps,
+        "clocks": clk,
+    }
+
+
 # ------------------------------------------------------------------ our arm: decode loops
 
 def run_loop(args, rank, world, local, key):
@@ -608,7 +710,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="smooth_step", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="smooth_step",
+                    choices=sorted(WORKLOADS) + ["tp8_shards"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -622,6 +725,8 @@ def main():
     cuda_build.build()
     if args.workload == "smooth_step":
         res = run_smooth_step(args, rank, world, local)
+    elif args.workload == "tp8_shards":
+        res = run_tp_shards(args, rank, world, local)
     else:
         res = run_loop(args, rank, world, local, args.workload)
     if rank == 0:
