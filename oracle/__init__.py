@@ -52,10 +52,16 @@ def _load():
         _lib.orc_round_to_bf16.argtypes = [vp, i64, vp]
         _lib.orc_kv_refresh.argtypes = [i32, i32, vp, i32, i32, vp, vp, vp]
         _lib.orc_merge_shard_stats.argtypes = [i32, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+        _lib.orc_commit_hierarchical_levels.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, vp,
+                                                        dbl, i32, i32]
+        _lib.orc_commit_credit_tracked.argtypes = [i32, i32, vp, i32, i64, i64, vp, vp, vp, vp,
+                                                   vp, vp, vp, vp, vp, vp, i32, dbl, dbl, dbl,
+                                                   i32, vp, vp]
         for name in ("orc_stats", "orc_active_rows", "orc_commit_threshold",
                      "orc_commit_hierarchical", "orc_commit_credit", "orc_smooth_rows",
                      "orc_smooth_embed", "orc_prob_row_bf16", "orc_round_to_bf16",
-                     "orc_kv_refresh", "orc_merge_shard_stats"):
+                     "orc_kv_refresh", "orc_merge_shard_stats",
+                     "orc_commit_hierarchical_levels", "orc_commit_credit_tracked"):
             getattr(_lib, name).restype = ctypes.c_int
     return _lib
 
@@ -165,6 +171,34 @@ def commit_credit(st: BlockState, conf: np.ndarray, argmax: np.ndarray, decay: f
                                    float(boost), float(tau), int(eos_id), _p(score))
     _check(rc, "commit_credit")
     return score
+
+
+def commit_hierarchical_levels(st: BlockState, conf: np.ndarray, argmax: np.ndarray,
+                               tau_low: float, min_width: int, eos_id: int = -1) -> None:
+    conf = np.ascontiguousarray(conf, np.float64)
+    argmax = np.ascontiguousarray(argmax, np.int32)
+    rc = _load().orc_commit_hierarchical_levels(st.B, st.L, _p(conf), _p(argmax), _p(st.masked),
+                                                _p(st.tokens), _p(st.committed_now),
+                                                _p(st.n_commit), _p(st.eos_hit), float(tau_low),
+                                                int(min_width), int(eos_id))
+    _check(rc, "commit_hierarchical_levels")
+
+
+def commit_credit_tracked(st: BlockState, logits: np.ndarray, s: "Stats", decay: float,
+                          boost: float, tau: float, eos_id: int = -1):
+    """Returns (boosted score, candidate token) of every row (0 / -1 for rows not read)."""
+    lg = np.ascontiguousarray(logits)
+    V = lg.shape[-1]
+    score = np.zeros((st.B, st.L), np.float64)
+    token = np.full((st.B, st.L), -1, np.int32)
+    rc = _load().orc_commit_credit_tracked(
+        st.B, st.L, _p(lg), _dtype_code(lg), V, V, _p(np.ascontiguousarray(s.lse, np.float64)),
+        _p(np.ascontiguousarray(s.conf, np.float64)), _p(np.ascontiguousarray(s.argmax, np.int32)),
+        _p(st.masked), _p(st.tokens), _p(st.committed_now), _p(st.n_commit), _p(st.eos_hit),
+        _p(st.cand_id), _p(st.cand_credit), st.K, float(decay), float(boost), float(tau),
+        int(eos_id), _p(score), _p(token))
+    _check(rc, "commit_credit_tracked")
+    return score, token
 
 
 def smooth_rows(masked: np.ndarray, eos_hit: np.ndarray) -> np.ndarray:

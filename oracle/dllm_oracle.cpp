@@ -111,6 +111,27 @@ void halve(int s, int e, int min_width, std::vector<int>* leaves) {
   }
 }
 
+// Node selections of the halving tree of run [s, e) (see orc_commit_hierarchical_levels).
+void select_levels(int s, int e, int min_width, const double* cf, double tau_low,
+                   std::vector<uint8_t>* sel) {
+  int best = -1, best_dist = 0;
+  for (int j = s; j < e; ++j) {
+    if (!(cf[j] >= tau_low)) continue;
+    const int dist = std::abs(2 * j - (s + e - 1));
+    if (best < 0 || dist < best_dist) {
+      best = j;
+      best_dist = dist;
+    }
+  }
+  if (best >= 0) (*sel)[best] = 1;
+  const int w = e - s;
+  if (w >= 2 * min_width) {
+    const int c = s + w / 2;
+    select_levels(s, c, min_width, cf, tau_low, sel);
+    select_levels(c, e, min_width, cf, tau_low, sel);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -288,6 +309,125 @@ int orc_commit_credit(int B, int L, const double* conf, const int32_t* argmax, u
       for (int i = 0; i < L; ++i) score_out[b * L + i] = 0.0;
     }
     apply_commits(L, commit, argmax + b * L, mk, tokens + b * L, committed_now + b * L,
+                  n_commit + b, eos_hit + b, eos_id);
+  }
+  return 0;
+}
+
+// Hierarchical decoding, a centre per level (variant of the function above; dInfer explainer,
+// decoding strategies, method 2, "decide each centre first" read as: every level's centre is
+// decided).  Every node [s, e) of the halving tree of each maximal masked run, internal or leaf,
+// selects its eligible position (conf >= tau_low) nearest its centre, |2j - (s + e - 1)|
+// smallest, lowest j on ties; the union of the selections is committed; fallback as above.
+// Written as a recursive walk over the tree's nodes.
+int orc_commit_hierarchical_levels(int B, int L, const double* conf, const int32_t* argmax,
+                                   uint8_t* masked, int32_t* tokens, uint8_t* committed_now,
+                                   int32_t* n_commit, int32_t* eos_hit, double tau_low,
+                                   int min_width, int eos_id) {
+  if (min_width < 1) return 1;
+  for (int b = 0; b < B; ++b) {
+    const double* cf = conf + b * L;
+    uint8_t* mk = masked + b * L;
+    std::vector<int> commit;
+    if (!sequence_stopped(L, mk, eos_hit + b)) {
+      std::vector<uint8_t> sel(L, 0);
+      int i = 0;
+      while (i < L) {
+        if (!mk[i]) {
+          ++i;
+          continue;
+        }
+        const int s = i;
+        while (i < L && mk[i]) ++i;
+        select_levels(s, i, min_width, cf, tau_low, &sel);
+      }
+      for (int j = 0; j < L; ++j)
+        if (sel[j]) commit.push_back(j);
+      if (commit.empty()) commit.push_back(masked_argmax(L, mk, cf));
+    }
+    apply_commits(L, commit, argmax + b * L, mk, tokens + b * L, committed_now + b * L,
+                  n_commit + b, eos_hit + b, eos_id);
+  }
+  return 0;
+}
+
+// Credit decoding, every tracked candidate credited (variant of orc_commit_credit; dInfer
+// explainer, decoding strategies, method 3).  Per masked position with probabilities
+// p_v = exp(z_v - lse) (z read from the logits, lse from orc_stats), top token a, p_a = conf:
+//   c_k <- decay * c_k for every slot; c_k <- c_k + p_{id_k} for every occupied slot;
+//   a not tracked: first empty slot, else evict the least credit (after the gains; lowest slot
+//   on ties), starting at p_a;
+//   s_k = p_{id_k} * (1 + boost * ln(1 + c_k)) over occupied slots; the best slot (lowest slot
+//   on ties) gives the position's score and token; commit if score > tau; fallback: best score.
+// token_out (nullable) receives the candidate token of every active row (-1 elsewhere).
+int orc_commit_credit_tracked(int B, int L, const void* logits, int dtype, int64_t V,
+                              int64_t row_stride, const double* lse, const double* conf,
+                              const int32_t* argmax, uint8_t* masked, int32_t* tokens,
+                              uint8_t* committed_now, int32_t* n_commit, int32_t* eos_hit,
+                              int32_t* cand_id, double* cand_credit, int K, double decay,
+                              double boost, double tau, int eos_id, double* score_out,
+                              int32_t* token_out) {
+  if (K < 1 || !logits || V <= 0 || row_stride < V) return 1;
+  const int64_t esize = dtype == 0 ? 4 : 2;
+  std::vector<double> score(L);
+  std::vector<int32_t> token(L);
+  for (int b = 0; b < B; ++b) {
+    const double* cf = conf + b * L;
+    uint8_t* mk = masked + b * L;
+    std::vector<int> commit;
+    const bool stopped = sequence_stopped(L, mk, eos_hit + b);
+    for (int i = 0; i < L; ++i) {
+      score[i] = 0.0;
+      token[i] = -1;
+      if (stopped || !mk[i]) continue;
+      const int64_t r = static_cast<int64_t>(b) * L + i;
+      const void* row = static_cast<const char*>(logits) + r * row_stride * esize;
+      int32_t* ids = cand_id + r * K;
+      double* cr = cand_credit + r * K;
+      const int32_t a = argmax[r];
+      for (int k = 0; k < K; ++k) {
+        cr[k] = decay * cr[k];
+        if (ids[k] >= 0) cr[k] += std::exp(load_logit(row, dtype, ids[k]) - lse[r]);
+      }
+      bool tracked = false;
+      for (int k = 0; k < K; ++k)
+        if (ids[k] == a) tracked = true;
+      if (!tracked) {
+        int slot = -1;
+        for (int k = 0; k < K && slot < 0; ++k)
+          if (ids[k] == -1) slot = k;
+        if (slot < 0) {
+          slot = 0;
+          for (int k = 1; k < K; ++k)
+            if (cr[k] < cr[slot]) slot = k;
+        }
+        ids[slot] = a;
+        cr[slot] = cf[i];
+      }
+      int best = -1;
+      double best_s = 0.0;
+      for (int k = 0; k < K; ++k) {
+        if (ids[k] < 0) continue;
+        const double p = std::exp(load_logit(row, dtype, ids[k]) - lse[r]);
+        const double sk = p * (1.0 + boost * std::log1p(cr[k]));
+        if (best < 0 || sk > best_s) {
+          best = k;
+          best_s = sk;
+        }
+      }
+      score[i] = best_s;
+      token[i] = ids[best];
+    }
+    if (!stopped) {
+      for (int i = 0; i < L; ++i)
+        if (mk[i] && score[i] > tau) commit.push_back(i);
+      if (commit.empty()) commit.push_back(masked_argmax(L, mk, score.data()));
+    }
+    if (score_out)
+      for (int i = 0; i < L; ++i) score_out[b * L + i] = score[i];
+    if (token_out)
+      for (int i = 0; i < L; ++i) token_out[b * L + i] = token[i];
+    apply_commits(L, commit, token.data(), mk, tokens + b * L, committed_now + b * L,
                   n_commit + b, eos_hit + b, eos_id);
   }
   return 0;
