@@ -62,6 +62,15 @@ _SIGS = {
                                           ctypes.POINTER(dllm_stats),
                                           ctypes.POINTER(dllm_block_state), _c_f32, _c_i32,
                                           _c_i32, _c_vp, _c_vp]),
+    "dllm_commit_hierarchical_levels": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape),
+                                                 ctypes.POINTER(dllm_stats),
+                                                 ctypes.POINTER(dllm_block_state), _c_f32,
+                                                 _c_i32, _c_i32, _c_vp, _c_vp]),
+    "dllm_commit_credit_tracked": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape),
+                                            ctypes.POINTER(dllm_stats),
+                                            ctypes.POINTER(dllm_block_state), _c_vp, _c_vp,
+                                            _c_i32, _c_f32, _c_f32, _c_f32, _c_i32, _c_vp,
+                                            _c_vp]),
     "dllm_commit_credit": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape),
                                     ctypes.POINTER(dllm_stats), ctypes.POINTER(dllm_block_state),
                                     _c_vp, _c_vp, _c_i32, _c_f32, _c_f32, _c_f32, _c_i32, _c_vp,
@@ -223,6 +232,27 @@ def dllm_commit_hierarchical(logits, shape, stats: StatsBuffers, state: BlockSta
                                           ctypes.byref(bs), tau_low, min_width, eos_id, _ptr(ws),
                                           _stream(stream)),
            "dllm_commit_hierarchical")
+
+
+def dllm_commit_hierarchical_levels(logits, shape, stats: StatsBuffers, state: BlockState,
+                                    tau_low: float, min_width: int, eos_id: int, ws,
+                                    stream=None) -> None:
+    st, bs = stats.c(), state.c()
+    _check(lib().dllm_commit_hierarchical_levels(_ptr(logits), ctypes.byref(shape),
+                                                 ctypes.byref(st), ctypes.byref(bs), tau_low,
+                                                 min_width, eos_id, _ptr(ws), _stream(stream)),
+           "dllm_commit_hierarchical_levels")
+
+
+def dllm_commit_credit_tracked(logits, shape, stats: StatsBuffers, state: BlockState, K: int,
+                               decay: float, boost: float, tau: float, eos_id: int, ws,
+                               stream=None) -> None:
+    st, bs = stats.c(), state.c()
+    _check(lib().dllm_commit_credit_tracked(_ptr(logits), ctypes.byref(shape), ctypes.byref(st),
+                                            ctypes.byref(bs), _ptr(state.cand_id),
+                                            _ptr(state.cand_credit), K, decay, boost, tau, eos_id,
+                                            _ptr(ws), _stream(stream)),
+           "dllm_commit_credit_tracked")
 
 
 def dllm_commit_credit(logits, shape, stats: StatsBuffers, state: BlockState, K: int,

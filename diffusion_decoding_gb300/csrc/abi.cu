@@ -189,6 +189,46 @@ dllm_status dllm_commit_credit(const void* logits, const dllm_shape* shape,
   return commit_common(logits, shape, stats, state, ca, ws, stream, "dllm_commit_credit");
 }
 
+dllm_status dllm_commit_hierarchical_levels(const void* logits, const dllm_shape* shape,
+                                            const dllm_stats* stats,
+                                            const dllm_block_state* state, float tau_low,
+                                            int32_t min_width, int32_t eos_id, void* ws,
+                                            dllm_stream_t stream) {
+  if (min_width < 1) return fail(DLLM_ERR_INVALID_ARG, "min_width must be >= 1");
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kHierarchicalLevels;
+  ca.tau_low = tau_low;
+  ca.min_width = min_width;
+  ca.eos_id = eos_id;
+  return commit_common(logits, shape, stats, state, ca, ws, stream,
+                       "dllm_commit_hierarchical_levels");
+}
+
+dllm_status dllm_commit_credit_tracked(const void* logits, const dllm_shape* shape,
+                                       const dllm_stats* stats, const dllm_block_state* state,
+                                       int32_t* cand_id, float* cand_credit, int32_t K,
+                                       float decay, float boost, float tau, int32_t eos_id,
+                                       void* ws, dllm_stream_t stream) {
+  if (!logits)
+    return fail(DLLM_ERR_INVALID_ARG,
+                "logits is null (the tracked-credit variant reads every tracked token's logit)");
+  if (!cand_id || !cand_credit)
+    return fail(DLLM_ERR_INVALID_ARG, "cand_id and cand_credit must not be null");
+  if (K < 1 || K > dllm::kMaxK)
+    return fail(K < 1 ? DLLM_ERR_INVALID_ARG : DLLM_ERR_UNSUPPORTED, "K=%d outside [1, %d]", K,
+                dllm::kMaxK);
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kCreditTracked;
+  ca.tau = tau;
+  ca.eos_id = eos_id;
+  ca.cand_id = cand_id;
+  ca.cand_credit = cand_credit;
+  ca.K = K;
+  ca.decay = decay;
+  ca.boost = boost;
+  return commit_common(logits, shape, stats, state, ca, ws, stream, "dllm_commit_credit_tracked");
+}
+
 size_t dllm_embedding_t_elems(int32_t V, int32_t d) {
   if (V < 1 || d < 1) return 0;
   return static_cast<size_t>(d) * dllm::align_up(static_cast<size_t>(V), 64);

@@ -12,7 +12,14 @@ namespace dllm {
 constexpr int kMaxL = 1024;
 constexpr int kMaxK = 16;
 
-enum CommitMode { kStatsOnly = 0, kThreshold = 1, kHierarchical = 2, kCredit = 3 };
+enum CommitMode {
+  kStatsOnly = 0,
+  kThreshold = 1,
+  kHierarchical = 2,
+  kCredit = 3,
+  kHierarchicalLevels = 4,  // variant: a centre per level of the halving tree
+  kCreditTracked = 5,       // variant: every tracked candidate gains its own probability
+};
 
 struct CommitArgs {
   int mode;
@@ -25,6 +32,11 @@ struct CommitArgs {
   int K;
   float decay;
   float boost;
+  // kCreditTracked reads the logits of the tracked tokens (set by the launcher)
+  const char* logits;
+  int64_t row_stride_bytes;
+  int dtype;
+  const float* lse;
 };
 
 // Stats/commit workspace layout.

@@ -281,15 +281,17 @@ __device__ int block_masked_argmax(const float* val, const uint8_t* mask, int L)
 
 struct EpiSmem {
   float* val;      // ranking value: confidence, or boosted score for credit decoding
-  int* am;         // argmax token of each position
+  int* am;         // token committed if the position is chosen (the argmax, or the best
+                   // tracked candidate for the tracked-credit variant)
   int* scan1;      // hierarchical: last unmasked index <= i
   int* scan2;      // hierarchical: same on the reversed block
   int* key;        // hierarchical: best (distance, index) key per leaf start
+  int* keyi;       // hierarchical, a centre per level: same per internal node, at its cut
   uint8_t* mask;   // masked bits at the start of the step
   uint8_t* sel;    // positions committed in this step
 };
 
-__host__ __device__ inline size_t epi_smem_bytes(int L) { return static_cast<size_t>(L) * 22 + 64; }
+__host__ __device__ inline size_t epi_smem_bytes(int L) { return static_cast<size_t>(L) * 26 + 64; }
 
 __device__ EpiSmem carve(uint8_t* dyn, int L) {
   EpiSmem s;
@@ -298,9 +300,39 @@ __device__ EpiSmem carve(uint8_t* dyn, int L) {
   s.scan1 = reinterpret_cast<int*>(dyn + 8 * L);
   s.scan2 = reinterpret_cast<int*>(dyn + 12 * L);
   s.key = reinterpret_cast<int*>(dyn + 16 * L);
-  s.mask = dyn + 20 * L;
-  s.sel = dyn + 21 * L;
+  s.keyi = reinterpret_cast<int*>(dyn + 20 * L);
+  s.mask = dyn + 24 * L;
+  s.sel = dyn + 25 * L;
   return s;
+}
+
+// Walk position i's path through the halving tree of its run, from the run down to its leaf,
+// calling f(key_slot, key) at every node: internal nodes are identified by their cut (keyi),
+// leaves by their start (key); key = distance to the node centre * 2048 + i.
+template <typename F>
+__device__ __forceinline__ void walk_levels(const EpiSmem& sm, int L, int min_width, int i,
+                                            F f) {
+  int s = sm.scan1[i] + 1;
+  const int j = sm.scan2[L - 1 - i];
+  int e = (j < 0) ? L : (L - 1 - j);
+  for (;;) {
+    const int k = abs(2 * i - (s + e - 1)) * 2048 + i;
+    if (e - s >= 2 * min_width) {
+      const int cut = s + (e - s) / 2;
+      f(&sm.keyi[cut], k);
+      if (i < cut) e = cut; else s = cut;
+    } else {
+      f(&sm.key[s], k);
+      return;
+    }
+  }
+}
+
+// Probability of token id in row r (tracked-credit variant): exp(z_id - lse_r).
+__device__ __forceinline__ float token_prob(const CommitArgs& ca, int64_t r, int id, float lse) {
+  const char* row = ca.logits + r * ca.row_stride_bytes;
+  const float z = load_logit(row, ca.dtype, id);
+  return ex2((z - lse) * kLog2e);
 }
 
 // Leaf [s, e) of the recursive halving that contains masked position i (hierarchical decoding).
@@ -331,7 +363,83 @@ __device__ void commit_sequence(const CommitCtx& c, int b, bool stopped, const E
     return;
   }
   const int mode = c.ca.mode;
-  if (mode == kThreshold) {
+  if (mode == kCreditTracked) {
+    const int K = c.ca.K;
+    for (int i = tid; i < L; i += nt) {
+      sm.sel[i] = 0;
+      if (!sm.mask[i]) continue;
+      const int64_t r = r0 + i;
+      int32_t* ids = c.ca.cand_id + r * K;
+      float* cr = c.ca.cand_credit + r * K;
+      const int a = sm.am[i];
+      const float pa = sm.val[i];
+      const float lse = __ldcg(c.ca.lse + r);
+      int id[kMaxK];
+      float cc[kMaxK], pk[kMaxK];
+      bool tracked = false;
+      for (int k = 0; k < K; ++k) {
+        id[k] = ids[k];
+        cc[k] = cr[k] * c.ca.decay;
+        pk[k] = 0.f;
+        if (id[k] >= 0) {
+          pk[k] = token_prob(c.ca, r, id[k], lse);
+          cc[k] += pk[k];
+        }
+        if (id[k] == a) tracked = true;
+      }
+      if (!tracked) {
+        int slot = -1;
+        for (int k = 0; k < K && slot < 0; ++k)
+          if (id[k] == -1) slot = k;
+        if (slot < 0) {
+          slot = 0;
+          for (int k = 1; k < K; ++k)
+            if (cc[k] < cc[slot]) slot = k;
+        }
+        id[slot] = a;
+        cc[slot] = pa;
+        pk[slot] = token_prob(c.ca, r, a, lse);
+      }
+      int best = -1;
+      float best_s = 0.f;
+      for (int k = 0; k < K; ++k) {
+        ids[k] = id[k];
+        cr[k] = cc[k];
+        if (id[k] < 0) continue;
+        const float sk = pk[k] * (1.f + c.ca.boost * log1pf(cc[k]));
+        if (best < 0 || sk > best_s) {
+          best = k;
+          best_s = sk;
+        }
+      }
+      sm.val[i] = best_s;
+      sm.am[i] = id[best];
+      sm.sel[i] = best_s > c.ca.tau ? 1 : 0;
+    }
+  } else if (mode == kHierarchicalLevels) {
+    for (int i = tid; i < L; i += nt) {
+      sm.scan1[i] = sm.mask[i] ? -1 : i;
+      sm.scan2[i] = sm.mask[L - 1 - i] ? -1 : i;
+      sm.key[i] = INT_MAX;
+      sm.keyi[i] = INT_MAX;
+    }
+    __syncthreads();
+    block_max_scan(sm.scan1, L);
+    block_max_scan(sm.scan2, L);
+    const int mw = c.ca.min_width;
+    for (int i = tid; i < L; i += nt) {
+      if (!sm.mask[i] || !(sm.val[i] >= c.ca.tau_low)) continue;
+      walk_levels(sm, L, mw, i, [](int* slot, int k) { atomicMin(slot, k); });
+    }
+    __syncthreads();
+    for (int i = tid; i < L; i += nt) {
+      sm.sel[i] = 0;
+      if (!sm.mask[i] || !(sm.val[i] >= c.ca.tau_low)) continue;
+      int won = 0;
+      walk_levels(sm, L, mw, i, [&won](int* slot, int k) { won |= (*slot == k); });
+      sm.sel[i] = won ? 1 : 0;
+    }
+  } else if (mode == kThreshold) {
     for (int i = tid; i < L; i += nt) sm.sel[i] = (sm.mask[i] && sm.val[i] > c.ca.tau) ? 1 : 0;
   } else if (mode == kCredit) {
     const int K = c.ca.K;
@@ -663,6 +771,10 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   p.c.B = sh.B;
   p.c.L = sh.L;
   p.c.ca = ca;
+  p.c.ca.logits = static_cast<const char*>(logits);
+  p.c.ca.row_stride_bytes = p.row_stride_bytes;
+  p.c.ca.dtype = sh.dtype;
+  p.c.ca.lse = stats.lse;
   if (ca.mode == kStatsOnly) {
     p.masked = masked;
     p.eos_hit = nullptr;

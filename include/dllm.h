@@ -166,6 +166,40 @@ dllm_status dllm_commit_credit(const void* logits, const dllm_shape* shape,
                                dllm_stream_t stream);
 
 /*
+ * Hierarchical decoding, a centre per level (variant of dllm_commit_hierarchical; the pages'
+ * "decide the centre of each sub-region first" read as deciding every level's centre).  Same
+ * halving tree; every node [s, e), internal or leaf, selects its position with
+ * conf >= tau_low closest to the node centre (smallest |2i - (s+e-1)|, lowest i on ties) and
+ * the union of the selections is committed; fallback, arguments and errors as
+ * dllm_commit_hierarchical.
+ */
+dllm_status dllm_commit_hierarchical_levels(const void* logits, const dllm_shape* shape,
+                                            const dllm_stats* stats,
+                                            const dllm_block_state* state, float tau_low,
+                                            int32_t min_width, int32_t eos_id, void* ws,
+                                            dllm_stream_t stream);
+
+/*
+ * Credit decoding, every tracked candidate credited (variant of dllm_commit_credit; dInfer
+ * explainer, decoding strategies, method 3).  Per masked position of a running sequence, with
+ * p_v = exp(z_v - lse), top token a and p_a = conf:
+ *   every slot decays, c_k <- decay*c_k;  every occupied slot gains its own token's probability,
+ *   c_k <- c_k + p_{id_k};  if a is not tracked it takes the first empty slot, or evicts the
+ *   slot of least credit (after the gains; lowest slot on ties), starting at p_a;
+ *   s_k = p_{id_k} * (1 + boost * ln(1 + c_k)) over occupied slots; the best slot (lowest slot on
+ *   ties) is the position's candidate: score = s_k, token = id_k (may differ from a);
+ *   C = { i : score_i > tau }, or the masked i of largest score (lowest i); commits the
+ *   candidate tokens.
+ * logits must not be NULL (the tracked tokens' logits are read after the statistics).  Other
+ * arguments and errors as dllm_commit_credit.
+ */
+dllm_status dllm_commit_credit_tracked(const void* logits, const dllm_shape* shape,
+                                       const dllm_stats* stats, const dllm_block_state* state,
+                                       int32_t* cand_id, float* cand_credit, int32_t K,
+                                       float decay, float boost, float tau, int32_t eos_id,
+                                       void* ws, dllm_stream_t stream);
+
+/*
  * Re-lay the embedding table once for the smoothing GEMM: E [V, d] bf16 row-major (the usual
  * table) -> Et, the transpose stored K-slab-blocked: Et[(v / 64) * d + c][v % 64] = E[v][c], so
  * that each 64-wide slab of the vocabulary is contiguous for every column c; slab entries with

@@ -33,6 +33,12 @@ class GpuDecoder:
         elif w.strategy == "hierarchical":
             dd.dllm_commit_hierarchical(logits_dev, self.shape, self.stats, self.state, w.tau_low,
                                         w.min_width, w.eos_id, self.ws)
+        elif w.strategy == "hierarchical_levels":
+            dd.dllm_commit_hierarchical_levels(logits_dev, self.shape, self.stats, self.state,
+                                               w.tau_low, w.min_width, w.eos_id, self.ws)
+        elif w.strategy == "credit_tracked":
+            dd.dllm_commit_credit_tracked(logits_dev, self.shape, self.stats, self.state, w.K,
+                                          w.decay, w.boost, w.tau, w.eos_id, self.ws)
         else:
             dd.dllm_commit_credit(logits_dev, self.shape, self.stats, self.state, w.K, w.decay,
                                   w.boost, w.tau, w.eos_id, self.ws)

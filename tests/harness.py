@@ -28,7 +28,42 @@ def _gap_ok(values: np.ndarray) -> bool:
     return top2[1] - top2[0] >= MARGIN * top2[1]
 
 
-def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray) -> bool:
+def _tracked_margins_ok(w, st: oracle.BlockState, lg: np.ndarray, s) -> bool:
+    """Tracked-credit variant: the slot to evict (credits after the gains) and the best tracked
+    candidate (per-slot boosted scores) must both be separated from the runner-up."""
+    B, L, K = st.B, st.L, st.K
+    V = lg.shape[-1]
+    rows = lg.reshape(B * L, V)
+    decay, boost = float(np.float32(w.decay)), float(np.float32(w.boost))
+    trial = st.copy()
+    oracle.commit_credit_tracked(trial, lg, s, decay, boost, float(np.float32(w.tau)))
+    for b in range(B):
+        if st.eos_hit[b] or not st.masked[b].any():
+            continue
+        for i in np.nonzero(st.masked[b])[0]:
+            r = b * L + i
+            if rows.dtype == np.uint16:  # bf16 bit patterns
+                row = (rows[r].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            else:
+                row = rows[r].astype(np.float64)
+            ids = st.cand_id[b, i]
+            p_of = lambda v: float(np.exp(row[v] - s.lse[r]))
+            a = int(s.argmax[r])
+            if a not in ids and not (ids == -1).any():
+                gained = [decay * st.cand_credit[b, i, k] + p_of(ids[k]) for k in range(K)]
+                g = np.sort(gained)
+                if g[1] - g[0] < EVICT_MARGIN * max(g[1], 1e-30):
+                    return False
+            tid, tc = trial.cand_id[b, i], trial.cand_credit[b, i]
+            sc = np.sort([p_of(tid[k]) * (1 + boost * np.log1p(tc[k]))
+                          for k in range(K) if tid[k] >= 0])
+            if len(sc) > 1 and sc[-1] - sc[-2] < EVICT_MARGIN * sc[-1]:
+                return False
+    return True
+
+
+def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray,
+               lg: np.ndarray | None = None, s=None) -> bool:
     """Check the guard for one step of workload w from oracle state st (not mutated)."""
     B, L = st.B, st.L
     conf = conf.reshape(B, L)
@@ -38,6 +73,13 @@ def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray) -
         trial = st.copy()
         scores = oracle.commit_credit(trial, conf, argmax, float(np.float32(w.decay)),
                                       float(np.float32(w.boost)), float(np.float32(w.tau)))
+    elif w.strategy == "credit_tracked":
+        if not _tracked_margins_ok(w, st, lg, s):
+            return False
+        trial = st.copy()
+        scores, _ = oracle.commit_credit_tracked(trial, lg, s, float(np.float32(w.decay)),
+                                                 float(np.float32(w.boost)),
+                                                 float(np.float32(w.tau)))
     for b in range(B):
         m = (st.masked[b] == 1) & (st.eos_hit[b] == 0)
         if not m.any():
@@ -48,7 +90,7 @@ def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray) -
                 return False
             if not np.any(c > w.tau) and not _gap_ok(c):
                 return False
-        elif w.strategy == "hierarchical":
+        elif w.strategy in ("hierarchical", "hierarchical_levels"):
             tl = float(np.float32(w.tau_low))
             if np.any(np.abs(c - tl) < MARGIN):
                 return False
@@ -56,13 +98,13 @@ def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray) -
             # no masked position is eligible
             if not np.any(c >= tl) and not _gap_ok(c):
                 return False
-        elif w.strategy == "credit":
+        elif w.strategy in ("credit", "credit_tracked"):
             s = scores[b][m]
             if np.any(np.abs(s - float(np.float32(w.tau))) < MARGIN):
                 return False
             if not np.any(s > w.tau) and not _gap_ok(s):
                 return False
-            for i in np.nonzero(m)[0]:
+            for i in np.nonzero(m)[0] if w.strategy == "credit" else []:
                 ids = st.cand_id[b, i]
                 if argmax[b, i] in ids or (ids == -1).any():
                     continue
@@ -84,6 +126,13 @@ def oracle_step(w, st: oracle.BlockState, lg: np.ndarray, s=None):
     elif w.strategy == "hierarchical":
         oracle.commit_hierarchical(st, conf, am, float(np.float32(w.tau_low)), w.min_width,
                                    w.eos_id)
+    elif w.strategy == "hierarchical_levels":
+        oracle.commit_hierarchical_levels(st, conf, am, float(np.float32(w.tau_low)),
+                                          w.min_width, w.eos_id)
+    elif w.strategy == "credit_tracked":
+        scores, _ = oracle.commit_credit_tracked(st, lg, s, float(np.float32(w.decay)),
+                                                 float(np.float32(w.boost)),
+                                                 float(np.float32(w.tau)), w.eos_id)
     else:
         scores = oracle.commit_credit(st, conf, am, float(np.float32(w.decay)),
                                       float(np.float32(w.boost)), float(np.float32(w.tau)),
@@ -98,7 +147,7 @@ def guarded_logits(w, seed: int, it: int, st: oracle.BlockState, calibrated: boo
         lg = synth.logits(w, seed, it, attempt, calibrated)
         act = oracle.active_rows(st.masked, st.eos_hit)
         s = oracle.stats(lg, act)
-        if margins_ok(w, st, s.conf, s.argmax):
+        if margins_ok(w, st, s.conf, s.argmax, lg, s):
             return lg, attempt, s
     raise RuntimeError(f"no draw satisfied the margin guard after {max_attempts} attempts")
 

@@ -1,0 +1,57 @@
+"""GPU vs oracle: the strategy variants (hierarchical with a centre per level; credit crediting
+every tracked candidate), over whole decode loops: commits, tokens and candidate slots bit-exact,
+credits within 2e-3, every iteration."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_runner import GpuDecoder, to_device
+from harness import close, guarded_logits, oracle_step
+
+import diffusion_decoding_gb300 as dd
+
+pytestmark = pytest.mark.gpu
+
+
+def _loop(w, seed, iters, calibrated):
+    gpu = GpuDecoder(w)
+    ost = oracle.BlockState(w.B, w.L, w.K)
+    for it in range(iters):
+        if not ost.masked.any():
+            break
+        lg, _, s = guarded_logits(w, seed, it, ost, calibrated)
+        oracle_step(w, ost, lg, s)
+        gpu.step(to_device(lg))
+        torch.cuda.synchronize()
+        hs = gpu.host_state()
+        for k in ("masked", "tokens", "committed_now", "n_commit", "eos_hit"):
+            assert np.array_equal(hs[k], getattr(ost, k)), (it, k)
+        if w.K:
+            assert np.array_equal(hs["cand_id"], ost.cand_id), it
+            assert close(hs["cand_credit"], ost.cand_credit), it
+    return ost
+
+
+@pytest.mark.parametrize("calibrated", [True, False])
+def test_hierarchical_levels_loop(calibrated):
+    w = synth.WORKLOADS["hierarchical_loop"].scaled(B=4, L=64, V=20000,
+                                                    strategy="hierarchical_levels")
+    st = _loop(w, seed=31, iters=64, calibrated=calibrated)
+    assert not st.masked.any()
+
+
+@pytest.mark.parametrize("calibrated", [True, False])
+def test_credit_tracked_loop(calibrated):
+    w = synth.WORKLOADS["credit_loop"].scaled(B=8, L=32, V=20000, strategy="credit_tracked",
+                                              max_iters=12)
+    _loop(w, seed=41, iters=12, calibrated=calibrated)
+
+
+def test_credit_tracked_needs_logits():
+    w = synth.WORKLOADS["credit_loop"].scaled(B=1, L=8, V=1024)
+    gpu = GpuDecoder(w)
+    with pytest.raises(dd.DllmError):
+        dd.dllm_commit_credit_tracked(None, gpu.shape, gpu.stats, gpu.state, w.K, w.decay,
+                                      w.boost, w.tau, -1, gpu.ws)
