@@ -551,6 +551,12 @@ def run_loop(args, rank, world, local, key):
         elif w.strategy == "hierarchical":
             dd.dllm_commit_hierarchical(lg, shape, stats, state, w.tau_low, w.min_width,
                                         w.eos_id, ws)
+        elif w.strategy == "hierarchical_levels":
+            dd.dllm_commit_hierarchical_levels(lg, shape, stats, state, w.tau_low, w.min_width,
+                                               w.eos_id, ws)
+        elif w.strategy == "credit_tracked":
+            dd.dllm_commit_credit_tracked(lg, shape, stats, state, w.K, w.decay, w.boost, w.tau,
+                                          w.eos_id, ws)
         else:
             dd.dllm_commit_credit(lg, shape, stats, state, w.K, w.decay, w.boost, w.tau,
                                   w.eos_id, ws)

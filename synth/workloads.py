@@ -12,7 +12,8 @@ from dataclasses import dataclass, replace
 class Workload:
     key: str
     title: str
-    strategy: str          # threshold | hierarchical | credit | smooth
+    strategy: str          # threshold | hierarchical | credit | smooth, or a variant:
+                           # hierarchical_levels | credit_tracked
     B: int
     L: int
     V: int
@@ -69,6 +70,20 @@ WORKLOADS = {
         title="threshold commit + iteration smoothing + KV refresh, B=16 L=64 V=126464 d=2048",
         strategy="smooth", B=16, L=64, V=126464, dtype="bf16", std=2.0, plant="none",
         tau=0.9, d=2048, prefix_len=1024, window=4, max_iters=1),
+    # the strategy variants (the readings the configured workloads do not take), at the
+    # hierarchical and credit shapes
+    "hierarchical_levels_loop": Workload(
+        key="hierarchical_levels_loop",
+        title="hierarchical decoding, a centre per level, to completion, B=8 L=64 V=126464 bf16",
+        strategy="hierarchical_levels", B=8, L=64, V=126464, dtype="bf16", std=2.0,
+        plant="fixed", peak_lo=2.0, peak_hi=12.0, tau_low=0.6, min_width=2, max_iters=64),
+    "credit_tracked_loop": Workload(
+        key="credit_tracked_loop",
+        title="credit decoding, every tracked candidate credited, 24 steps, B=32 L=32 "
+              "V=126464 bf16, K=8",
+        strategy="credit_tracked", B=32, L=32, V=126464, dtype="bf16", std=2.0, plant="stable",
+        peak_lo=2.0, peak_hi=12.0, p_stable=0.7, K=8, decay=0.7, boost=0.3, tau=0.9,
+        max_iters=24),
 }
 
 # fixed seeds per workload (1000 + position in the list)
