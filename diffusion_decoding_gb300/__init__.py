@@ -82,6 +82,11 @@ _SIGS = {
                                    ctypes.POINTER(dllm_block_state), _c_vp, _c_i32, _c_vp, _c_vp,
                                    _c_vp, _c_vp, _c_sz, _c_vp]),
     "dllm_smooth_plan_info": (_c_i32, [ctypes.POINTER(dllm_shape), _c_i32, _c_vp]),
+    "dllm_commit_threshold_smooth": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape),
+                                              ctypes.POINTER(dllm_stats),
+                                              ctypes.POINTER(dllm_block_state), _c_f32, _c_i32,
+                                              _c_vp, _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz,
+                                              _c_vp]),
     "dllm_smooth_probs": (_c_i32, [_c_vp, ctypes.POINTER(dllm_shape), ctypes.POINTER(dllm_stats),
                                    ctypes.POINTER(dllm_block_state), _c_i32, _c_vp, _c_vp, _c_vp,
                                    _c_sz, _c_vp]),
@@ -288,6 +293,17 @@ def dllm_smooth_embed(logits, shape, stats: StatsBuffers, state: BlockState, Et,
                                    ctypes.byref(bs), _ptr(Et), d, _ptr(out), _ptr(row_ids),
                                    _ptr(M), _ptr(ws), ws.numel(), _stream(stream)),
            "dllm_smooth_embed")
+
+
+def dllm_commit_threshold_smooth(logits, shape, stats: StatsBuffers, state: BlockState,
+                                 tau: float, eos_id: int, Et, d: int, out, row_ids, M, ws,
+                                 stream=None) -> None:
+    st, bs = stats.c(), state.c()
+    _check(lib().dllm_commit_threshold_smooth(_ptr(logits), ctypes.byref(shape), ctypes.byref(st),
+                                              ctypes.byref(bs), tau, eos_id, _ptr(Et), d,
+                                              _ptr(out), _ptr(row_ids), _ptr(M), _ptr(ws),
+                                              ws.numel(), _stream(stream)),
+           "dllm_commit_threshold_smooth")
 
 
 def dllm_smooth_plan_info(shape, d: int) -> dict:

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdllm.so")
-SOURCES = ["stats_commit.cu", "scan.cu", "smooth.cu", "abi.cu", "static_ws.cu"]
+SOURCES = ["stats_commit.cu", "stats_probs.cu", "scan.cu", "smooth.cu", "abi.cu",
+           "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -317,7 +317,7 @@ dllm_status dllm_smooth_gemm(const dllm_shape* shape, const uint16_t* Et, int32_
       reinterpret_cast<const uint16_t*>(static_cast<const char*>(ws) + pl.off_p);
   const char* why = "launch failed";
   const int ldt = static_cast<int>(dllm::align_up(static_cast<size_t>(shape->V), 8));
-  cudaError_t e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, M, ws,
+  cudaError_t e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, M, nullptr, ws,
                                            reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess)
     return fail(DLLM_ERR_CUDA, "dllm_smooth_gemm: %s: %s", why, cudaGetErrorString(e));
@@ -333,6 +333,57 @@ dllm_status dllm_smooth_embed(const void* logits, const dllm_shape* shape, const
     return fail(DLLM_ERR_INVALID_ARG, "Et and out must be 16-byte aligned");
   DLLM_TRY(dllm_smooth_probs(logits, shape, stats, state, d, row_ids, M, ws, ws_bytes, stream));
   return dllm_smooth_gemm(shape, Et, d, out, M, ws, ws_bytes, stream);
+}
+
+dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* shape,
+                                        const dllm_stats* stats, const dllm_block_state* state,
+                                        float tau, int32_t eos_id, const uint16_t* Et, int32_t d,
+                                        float* out, int32_t* row_ids, int32_t* M, void* ws,
+                                        size_t ws_bytes, dllm_stream_t stream) {
+  dllm::SmoothPlan pl;
+  DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
+  if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
+  DLLM_TRY(check_logits(logits));
+  DLLM_TRY(check_stats(stats));
+  DLLM_TRY(check_state(state));
+  if (!Et || !out || !row_ids || !M)
+    return fail(DLLM_ERR_INVALID_ARG, "Et, out, row_ids and M must not be null");
+  if (!aligned(Et, 16) || !aligned(out, 16))
+    return fail(DLLM_ERR_INVALID_ARG, "Et and out must be 16-byte aligned");
+  int C = 0, per = 0;
+  if (!dllm::stats_probs_split(shape->V, shape->dtype, &C, &per))
+    return fail(DLLM_ERR_UNSUPPORTED,
+                "V=%d is too long for one row per cluster of 8 CTAs; use dllm_commit_threshold "
+                "and dllm_smooth_embed", shape->V);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  uint16_t* P = reinterpret_cast<uint16_t*>(w + pl.off_p);
+  int32_t* rows = reinterpret_cast<int32_t*>(w + pl.off_rows);
+  int32_t* count = reinterpret_cast<int32_t*>(w + pl.off_count);
+  int32_t* inv = reinterpret_cast<int32_t*>(w + pl.off_inv);
+  int32_t* map = reinterpret_cast<int32_t*>(w + pl.off_map);
+  const int R_pad = pl.m_tiles * 128;
+  cudaError_t e = dllm::launch_read_rows(*state, shape->B, shape->L, rows, count, *stats, st);
+  if (e == cudaSuccess)
+    e = dllm::launch_stats_probs(logits, *shape, rows, count, *stats, P, R_pad,
+                                 static_cast<int32_t*>(ws), st);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_commit_threshold_smooth (statistics)");
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kThreshold;
+  ca.tau = tau;
+  ca.eos_id = eos_id;
+  e = dllm::launch_commit_only(*shape, *stats, *state, ca, st);
+  if (e == cudaSuccess)
+    e = dllm::launch_kept_rows_map(*state, shape->B, shape->L, row_ids, M, rows, count, inv, map,
+                                   st);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_commit_threshold_smooth (commit)");
+  const char* why = "launch failed";
+  const int ldt = static_cast<int>(dllm::align_up(static_cast<size_t>(shape->V), 8));
+  e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, count, map, ws, st, &why);
+  if (e != cudaSuccess)
+    return fail(DLLM_ERR_CUDA, "dllm_commit_threshold_smooth: %s: %s", why,
+                cudaGetErrorString(e));
+  return ok();
 }
 
 dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32_t L,

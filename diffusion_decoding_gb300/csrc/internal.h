@@ -65,6 +65,18 @@ cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,
 cudaError_t launch_compact_rows(const dllm_block_state& state, int B, int L, int32_t* row_ids,
                                 int32_t* M, cudaStream_t stream);
 
+// Single-read smoothing: rows read this step (before the commit; -inf statistics for the
+// others), the fused statistics + probability rows, and the kept-row map after the commit.
+cudaError_t launch_read_rows(const dllm_block_state& state, int B, int L, int32_t* rows,
+                             int32_t* count, const dllm_stats& stats, cudaStream_t stream);
+bool stats_probs_split(int V, int dtype, int* C, int* slabs_per_cta);
+cudaError_t launch_stats_probs(const void* logits, const dllm_shape& sh, const int32_t* rows,
+                               const int32_t* count, const dllm_stats& stats, uint16_t* P,
+                               int R_pad, int32_t* status, cudaStream_t stream);
+cudaError_t launch_kept_rows_map(const dllm_block_state& state, int B, int L, int32_t* row_ids,
+                                 int32_t* M, const int32_t* rows_read, const int32_t* count_read,
+                                 int32_t* inv, int32_t* map, cudaStream_t stream);
+
 cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int prefix_len,
                               int window, uint8_t* refresh, int32_t* idx, int32_t* count,
                               cudaStream_t stream);
@@ -83,6 +95,10 @@ struct SmoothPlan {
   size_t ws_bytes;
   size_t off_p;       // bf16 P, K-slab-blocked [ldp / 64][R_pad][64]
   size_t off_part;    // fp32 partials [split_k, R_pad, d]
+  size_t off_rows;    // single-read path: rows read [R], their count, kept index per row [R],
+  size_t off_count;   // and kept index per row read [R]
+  size_t off_inv;
+  size_t off_map;
 };
 
 SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count);
@@ -91,9 +107,10 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
                              const int32_t* row_ids, const int32_t* M, uint16_t* P, int R_pad,
                              int sm_count, cudaStream_t stream);
 
+// out row of P row j: row_map[j] (-1: not written) when row_map is not null, else j.
 cudaError_t launch_smooth_gemm(const SmoothPlan& plan, const uint16_t* P, const uint16_t* Et,
-                               int ldt, float* out, const int32_t* M, void* ws,
-                               cudaStream_t stream, const char** why);
+                               int ldt, float* out, const int32_t* M, const int32_t* row_map,
+                               void* ws, cudaStream_t stream, const char** why);
 
 cudaError_t launch_merge_shard_stats(const dllm_shard_stats* shards, int n, int64_t rows,
                                      const dllm_stats& out, cudaStream_t stream);

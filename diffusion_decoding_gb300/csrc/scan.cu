@@ -59,6 +59,56 @@ __global__ void __launch_bounds__(kScanThreads) compact_rows_kernel(const uint8_
   if (threadIdx.x == 0) *M = base;
 }
 
+// Rows a step reads (masked, sequence running), ascending: the single-read smoothing path's row
+// list, taken before the commit.  Rows not read get the -inf, -inf, 0, -1 statistics here.
+__global__ void __launch_bounds__(kScanThreads) read_rows_kernel(const uint8_t* masked,
+                                                                 const int32_t* eos_hit, int B,
+                                                                 int L, int32_t* rows,
+                                                                 int32_t* count, dllm_stats st) {
+  const int R = B * L;
+  int base = 0;
+  for (int r0 = 0; r0 < R; r0 += kScanThreads) {
+    const int r = r0 + threadIdx.x;
+    const int read = (r < R) && masked[r] && !eos_hit[r / L];
+    int total;
+    const int off = block_exclusive_count<kScanThreads>(read, &total);
+    if (read) {
+      rows[base + off] = r;
+    } else if (r < R) {
+      st.row_max[r] = -INFINITY;
+      st.lse[r] = -INFINITY;
+      st.conf[r] = 0.f;
+      st.argmax[r] = -1;
+    }
+    base += total;
+  }
+  if (threadIdx.x == 0) *count = base;
+}
+
+// After the commit: the rows kept for smoothing (row_ids, M, as compact_rows_kernel) and, for
+// each row read this step (rows_read[0..count_read)), its index among the kept rows or -1 if it
+// was just committed (map), through inv[r] = kept index of row r or -1.
+__global__ void __launch_bounds__(kScanThreads) kept_rows_map_kernel(
+    const uint8_t* masked, const int32_t* eos_hit, int B, int L, int32_t* row_ids, int32_t* M,
+    const int32_t* rows_read, const int32_t* count_read, int32_t* inv, int32_t* map) {
+  const int R = B * L;
+  int base = 0;
+  for (int r0 = 0; r0 < R; r0 += kScanThreads) {
+    const int r = r0 + threadIdx.x;
+    const int keep = (r < R) && masked[r] && !eos_hit[r / L];
+    int total;
+    const int off = block_exclusive_count<kScanThreads>(keep, &total);
+    if (keep) row_ids[base + off] = r;
+    if (r < R) inv[r] = keep ? base + off : -1;
+    base += total;
+  }
+  for (int k = base + threadIdx.x; k < R; k += kScanThreads) row_ids[k] = -1;
+  if (threadIdx.x == 0) *M = base;
+  __syncthreads();  // inv is complete (global writes of this CTA are visible to it)
+  const int n = *count_read;
+  for (int c = threadIdx.x; c < n; c += kScanThreads) map[c] = __ldcg(inv + rows_read[c]);
+}
+
 // One CTA per sequence.  cnt[x] = number of block positions < x committed in this step; cache
 // position j is refreshed iff a committed block position lies in [j-P-w, j-P+w].
 __global__ void __launch_bounds__(kRefreshThreads) kv_refresh_kernel(const uint8_t* committed_now,
@@ -109,6 +159,22 @@ cudaError_t launch_compact_rows(const dllm_block_state& state, int B, int L, int
                                 int32_t* M, cudaStream_t stream) {
   compact_rows_kernel<<<1, kScanThreads, 0, stream>>>(state.masked, state.eos_hit, B, L, row_ids,
                                                       M);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_read_rows(const dllm_block_state& state, int B, int L, int32_t* rows,
+                             int32_t* count, const dllm_stats& stats, cudaStream_t stream) {
+  read_rows_kernel<<<1, kScanThreads, 0, stream>>>(state.masked, state.eos_hit, B, L, rows, count,
+                                                   stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kept_rows_map(const dllm_block_state& state, int B, int L, int32_t* row_ids,
+                                 int32_t* M, const int32_t* rows_read, const int32_t* count_read,
+                                 int32_t* inv, int32_t* map, cudaStream_t stream) {
+  kept_rows_map_kernel<<<1, kScanThreads, 0, stream>>>(state.masked, state.eos_hit, B, L,
+                                                       row_ids, M, rows_read, count_read, inv,
+                                                       map);
   return cudaGetLastError();
 }
 

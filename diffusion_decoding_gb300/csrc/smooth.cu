@@ -54,24 +54,6 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                : "memory");
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address of the same shared-memory location in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -175,6 +157,7 @@ struct GemmParams {
   float* out;          // [M, d] when split_k == 1
   float* part;         // [split_k, R_pad, d] otherwise
   const int32_t* M;
+  const int32_t* row_map;  // out row of P row j (-1: skipped); null: j itself
   int32_t* status;
 };
 
@@ -301,12 +284,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       float* dst_base = p.split_k == 1
                             ? p.out
                             : p.part + static_cast<size_t>(ks) * p.R_pad * p.d;
+      // split-K partials keep P's row order; the final rows are mapped by the reduction
+      const int orow = row >= Mdev ? -1
+                       : (p.split_k == 1 && p.row_map != nullptr) ? __ldg(p.row_map + row) : row;
       for (int c = 0; c < bn; c += 16) {
         uint32_t v[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
-        if (row < Mdev) {
+        if (orow >= 0) {
           float4* dst =
-              reinterpret_cast<float4*>(dst_base + static_cast<size_t>(row) * p.d + n0 + c);
+              reinterpret_cast<float4*>(dst_base + static_cast<size_t>(orow) * p.d + n0 + c);
           if (nkb == 0) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0u;
@@ -337,14 +323,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 }
 
 __global__ void splitk_reduce_kernel(const float* part, int split_k, int R_pad, int d,
-                                     const int32_t* M, float* out) {
+                                     const int32_t* M, const int32_t* row_map, float* out) {
   const int Mdev = *M;
-  const size_t n4 = static_cast<size_t>(Mdev) * d / 4;
-  const size_t slice = static_cast<size_t>(R_pad) * d / 4;
+  const int d4 = d / 4;
+  const size_t n4 = static_cast<size_t>(Mdev) * d4;
+  const size_t slice = static_cast<size_t>(R_pad) * d4;
   const float4* p4 = reinterpret_cast<const float4*>(part);
   float4* o4 = reinterpret_cast<float4*>(out);
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(i / d4);
+    const int orow = row_map != nullptr ? __ldg(row_map + row) : row;
+    if (orow < 0) continue;
     float4 acc = p4[i];
     for (int k = 1; k < split_k; ++k) {  // fixed order: deterministic
       const float4 v = p4[k * slice + i];
@@ -353,7 +343,7 @@ __global__ void splitk_reduce_kernel(const float* part, int split_k, int R_pad, 
       acc.z += v.z;
       acc.w += v.w;
     }
-    o4[i] = acc;
+    o4[static_cast<size_t>(orow) * d4 + (i - static_cast<size_t>(row) * d4)] = acc;
   }
 }
 
@@ -522,6 +512,16 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
   off = align_up(off, 1024);
   pl.off_part = off;
   if (pl.split_k > 1) off += static_cast<size_t>(pl.split_k) * R_pad * d * 4;
+  const size_t rows4 = align_up(4 * static_cast<size_t>(pl.R), 256);
+  off = align_up(off, 256);
+  pl.off_rows = off;
+  off += rows4;
+  pl.off_count = off;
+  off += 256;
+  pl.off_inv = off;
+  off += rows4;
+  pl.off_map = off;
+  off += rows4;
   pl.ws_bytes = align_up(off, 256);
   return pl;
 }
@@ -550,8 +550,8 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
 }
 
 cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const uint16_t* Et,
-                               int ldt, float* out, const int32_t* M, void* ws,
-                               cudaStream_t stream, const char** why) {
+                               int ldt, float* out, const int32_t* M, const int32_t* row_map,
+                               void* ws, cudaStream_t stream, const char** why) {
   const int R_pad = pl.m_tiles * kBM;
   (void)ldt;
   GemmParams gp{};
@@ -578,6 +578,7 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.out = out;
   gp.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.off_part);
   gp.M = M;
+  gp.row_map = row_map;
   gp.status = static_cast<int32_t*>(ws);
   const size_t smem = static_cast<size_t>(pl.stages) *
                           (kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2) + 1024;
@@ -591,7 +592,7 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   e = cudaGetLastError();
   if (e != cudaSuccess || pl.split_k == 1) return e;
   splitk_reduce_kernel<<<std::min(1024, std::max(1, pl.R * pl.d / 4 / 256)), 256, 0, stream>>>(
-      gp.part, pl.split_k, R_pad, pl.d, M, out);
+      gp.part, pl.split_k, R_pad, pl.d, M, row_map, out);
   return cudaGetLastError();
 }
 

@@ -1,12 +1,13 @@
 """Run one kernel family of the decode step a fixed number of times, for external profilers.
 
-    python -m diffusion_decoding_gb300.kernel_driver {stats|probs|gemm|step} [n]
+    python -m diffusion_decoding_gb300.kernel_driver {stats|probs|gemm|step|fused} [n]
 
 The inputs have the smoothing-step sizes (B=16, L=64, V=126464 bf16 logits, d=2048 embedding
 table; about 0.8 GB on the device), so every launch reads more than the L2 holds.  Nothing is
 timed here: a profiler (ncu) attaches to the launches.  `stats` runs the fused statistics +
 threshold commit; `probs` the probability rows; `gemm` the smoothing GEMM (after one
-probability pass); `step` the whole step (commit, probabilities, GEMM, KV refresh).
+probability pass); `step` the whole step (commit, probabilities, GEMM, KV refresh) through the
+separate calls; `fused` the whole step through the single-read call.
 """
 import sys
 
@@ -21,7 +22,7 @@ PREFIX, WINDOW, TAU = 1024, 4, 0.9
 def main(argv) -> None:
     what = argv[0] if argv else "step"
     n = int(argv[1]) if len(argv) > 1 else 4
-    if what not in ("stats", "probs", "gemm", "step"):
+    if what not in ("stats", "probs", "gemm", "step", "fused"):
         raise SystemExit(f"unknown kernel family {what!r}")
     dev = torch.device("cuda")
     g = torch.Generator(device=dev)
@@ -55,6 +56,11 @@ def main(argv) -> None:
             dd.dllm_smooth_probs(lg, shape, stats, state, D, row_ids, M, ws_s)
         elif what == "gemm":
             dd.dllm_smooth_gemm(shape, Et, D, out, M, ws_s)
+        elif what == "fused":
+            state.reset()
+            dd.dllm_commit_threshold_smooth(lg, shape, stats, state, TAU, -1, Et, D, out,
+                                            row_ids, M, ws_s)
+            dd.dllm_kv_refresh_mask(state, PREFIX, WINDOW, refresh, idx, count)
         else:
             state.reset()
             dd.dllm_commit_threshold(lg, shape, stats, state, TAU, -1, ws)

@@ -274,6 +274,24 @@ dllm_status dllm_merge_shard_stats(const dllm_shard_stats* shards, int32_t n, in
                                    const dllm_stats* out, dllm_stream_t stream);
 
 /*
+ * Threshold commit and iteration smoothing in one call, reading each logit from HBM once
+ * (single-read smoothing).  Results are those of dllm_commit_threshold followed by
+ * dllm_smooth_embed on the same arguments: the statistics of the rows read, the commit, and
+ * out[0..M) = P x E for the rows kept (row_ids ascending, M on the device), within the same
+ * tolerances.  The rows read are held on chip (a cluster of up to 8 CTAs per row, up to 192 KB
+ * per CTA) while their log-sum-exp completes, so their probabilities are written without a
+ * second read; the GEMM then covers the rows read (rows committed in this step included) and
+ * writes only the kept ones.
+ * ws: dllm_smooth_workspace_bytes(shape, d) bytes; Et prepared by dllm_prepare_embedding.
+ * V must be a multiple of 8; DLLM_ERR_UNSUPPORTED for V beyond 8 x 192 KB of one row.
+ */
+dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* shape,
+                                        const dllm_stats* stats, const dllm_block_state* state,
+                                        float tau, int32_t eos_id, const uint16_t* Et, int32_t d,
+                                        float* out, int32_t* row_ids, int32_t* M, void* ws,
+                                        size_t ws_bytes, dllm_stream_t stream);
+
+/*
  * Neighbourhood KV refresh (dInfer explainer, KV-cache manager: when a region of the sequence
  * changes, its cache entries and those of its neighbours are recomputed).  The cache row of
  * sequence b is [prefix 0..prefix_len) followed by the block, T = prefix_len + L entries:

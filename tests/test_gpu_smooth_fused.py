@@ -1,0 +1,83 @@
+"""GPU vs oracle: single-read smoothing (dllm_commit_threshold_smooth), the threshold commit and
+the iteration smoothing of one step with every logit read from HBM once."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_runner import GpuDecoder, to_device
+from harness import close, guarded_logits, oracle_step
+from test_gpu_smooth import _table, smooth_close
+
+import diffusion_decoding_gb300 as dd
+
+pytestmark = pytest.mark.gpu
+
+
+def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None):
+    gpu = GpuDecoder(w)
+    ost = oracle.BlockState(w.B, w.L)
+    if masked0 is not None:
+        ost.masked[:] = masked0
+        gpu.state.masked.copy_(torch.from_numpy(masked0.reshape(-1)).cuda())
+    lg, _, s = guarded_logits(w, seed, 0, ost, calibrated)
+    s_ref, _ = oracle_step(w, ost, lg, s)
+    E, Et = _table(w.V, w.d)
+    R = w.B * w.L
+    out = torch.full((R, w.d), float("nan"), dtype=torch.float32, device="cuda")
+    row_ids = torch.empty(R, dtype=torch.int32, device="cuda")
+    M = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
+    dt = dd.DLLM_BF16 if w.dtype == "bf16" else dd.DLLM_F32
+    dd.dllm_commit_threshold_smooth(to_device(lg), gpu.shape, gpu.stats, gpu.state, w.tau,
+                                    w.eos_id, Et, w.d, out, row_ids, M, ws)
+    torch.cuda.synchronize()
+    assert dd.dllm_get_status(ws) == dd.DLLM_OK
+    hs = gpu.host_state()
+    for k in ("masked", "tokens", "committed_now", "n_commit"):
+        assert np.array_equal(hs[k], getattr(ost, k)), k
+    st = gpu.host_stats()
+    assert np.array_equal(st["argmax"], s_ref.argmax)
+    assert np.array_equal(st["row_max"], s_ref.row_max.astype(np.float32))
+    for k in ("lse", "conf"):
+        assert close(st[k], getattr(s_ref, k)), k
+    ids_ref = oracle.smooth_rows(ost.masked, ost.eos_hit)
+    Mg = int(M.item())
+    assert Mg == len(ids_ref)
+    rid = row_ids.cpu().numpy()
+    assert np.array_equal(rid[:Mg], ids_ref) and (rid[Mg:] == -1).all()
+    o = out.cpu().numpy()
+    assert np.isnan(o[Mg:]).all(), "rows >= M must stay untouched"
+    js = np.arange(Mg) if sample_rows is None else np.unique(
+        np.linspace(0, Mg - 1, sample_rows).astype(int))
+    ids = ids_ref[js].astype(np.int32)
+    ref = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids, E)
+    scale = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids, E & np.uint16(0x7FFF))
+    smooth_close(o[js], ref, scale)
+    return Mg
+
+
+@pytest.mark.parametrize("B,L,V,d", [
+    (1, 8, 1024, 32),        # one CTA per row (no cluster exchange)
+    (3, 100, 2056, 160),     # ragged row tile, V not a multiple of 64
+    (2, 64, 20000, 272),     # clusters of 2 CTAs per row
+    (4, 64, 126464, 512),    # clusters of 8 CTAs per row (the full vocabulary)
+])
+def test_fused_small_all_rows(B, L, V, d):
+    w = synth.WORKLOADS["smooth_step"].scaled(B=B, L=L, V=V, d=d, prefix_len=16)
+    assert _fused_case(w, seed=B * 1000 + V, calibrated=True) > 0
+
+
+def test_fused_partial_mask_and_fp32():
+    w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=48, V=8192, d=64, dtype="f32",
+                                              prefix_len=8)
+    rng = np.random.default_rng(7)
+    m0 = (rng.random((w.B, w.L)) < 0.6).astype(np.uint8)
+    assert _fused_case(w, seed=5, calibrated=True, masked0=m0) > 0
+
+
+def test_fused_full_size_sampled_rows():
+    w = synth.WORKLOADS["smooth_step"]
+    Mg = _fused_case(w, synth.workloads.SEEDS[w.key], calibrated=False, sample_rows=6)
+    assert Mg == w.B * w.L - w.B
