@@ -26,7 +26,6 @@ constexpr int kSPThreads = 256;
 constexpr int kSPWarps = kSPThreads / 32;
 constexpr int kSPTargetBytes = 32768;       // slice of one CTA, aimed at
 constexpr int kSPMaxSliceBytes = 192 * 1024;
-constexpr int kCopyPiece = 16384;
 
 struct SPParams {
   const char* logits;
@@ -62,6 +61,44 @@ __device__ __forceinline__ void unpack_vec(const uint4& q, float* x) {
     x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y);
     x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
   }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Largest element of one 16-byte vector.
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& q) {
+  if constexpr (DT == DLLM_BF16) {
+    const uint32_t m = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
+    return fmaxf(bf16lo(m), bf16hi(m));
+  } else {
+    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+  }
+}
+
+// packed fp32 pairs for fma.rn.f32x2 / add.rn.f32x2
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 template <int DT>
@@ -120,12 +157,12 @@ template <int DT>
 __global__ void __launch_bounds__(kSPThreads, 4) stats_probs_kernel(const __grid_constant__ SPParams p) {
   using T = Elem<DT>;
   extern __shared__ __align__(128) uint8_t slice[];
-  __shared__ uint64_t bar;
   __shared__ float redf[kSPWarps];
   __shared__ int redi[kSPWarps];
   __shared__ float part_m, part_s;
   __shared__ int part_i;
-  __shared__ int abort_flag;
+  __shared__ float red_M, red_S;
+  __shared__ int red_I;
 
   const int tid = threadIdx.x;
   const uint32_t rank = p.C > 1 ? cluster_ctarank() : 0u;
@@ -136,24 +173,19 @@ __global__ void __launch_bounds__(kSPThreads, 4) stats_probs_kernel(const __grid
   const int n = max(0, min(p.V, e0 + p.slabs_per_cta * 64) - e0);  // elements of this slice
   const uint32_t sbase = smem_u32(slice);
 
-  // ---- the slice, by bulk copy (rounded up to 16 bytes: stays inside the row's stride)
-  if (tid == 0) {
-    mbar_init(smem_u32(&bar), 1);
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
+  // ---- the slice, by 16-byte cp.async from every thread (rounded up to 16 bytes: stays inside
+  // the row's stride).  (A single thread's bulk copy of the slice kept the kernel at ~4 TB/s.)
   const uint32_t bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(n) * T::ES, 16));
-  if (tid == 0) {
-    mbar_expect_tx(smem_u32(&bar), bytes);
+  {
     const char* src = p.logits + static_cast<int64_t>(r) * p.row_stride_bytes +
                       static_cast<int64_t>(e0) * T::ES;
-    for (uint32_t off = 0; off < bytes; off += kCopyPiece)
-      bulk_g2s(sbase + off, src + off, min(static_cast<uint32_t>(kCopyPiece), bytes - off),
-               smem_u32(&bar));
+    const int nchunks = static_cast<int>(bytes / 16);
+#pragma unroll 4
+    for (int i = tid; i < nchunks; i += kSPThreads) cp_async16(sbase + i * 16, src + i * 16);
+    cp_async_wait_all();
   }
-  const bool ok = wait_bar(smem_u32(&bar), 0, &abort_flag, p.status);
-  // (a failed wait still walks every barrier below, so the cluster never waits for this CTA)
+  __syncthreads();
+  const bool ok = true;
 
   // ---- pass 1: slice maximum and the first vector holding it, per thread, then per CTA
   const int nvec = n * T::ES / 16;
@@ -161,12 +193,9 @@ __global__ void __launch_bounds__(kSPThreads, 4) stats_probs_kernel(const __grid
   float tm = -INFINITY;
   int bu = -1;
   if (ok) {
+#pragma unroll 4
     for (int v = tid; v < nvec; v += kSPThreads) {
-      float x[T::VEC];
-      unpack_vec<DT>(ld_shared_v4(sbase + v * 16), x);
-      float vm = x[0];
-#pragma unroll
-      for (int k = 1; k < T::VEC; ++k) vm = fmaxf(vm, x[k]);
+      const float vm = vec_max<DT>(ld_shared_v4(sbase + v * 16));
       if (vm > tm) {
         tm = vm;
         bu = v;
@@ -198,12 +227,22 @@ __global__ void __launch_bounds__(kSPThreads, 4) stats_probs_kernel(const __grid
   float sum = 0.f;
   if (ok && mc != -INFINITY) {
     const float mb = mc * kLog2e;
+    const uint64_t k2 = pack2(kLog2e, kLog2e), nmb2 = pack2(-mb, -mb);
+    uint64_t acc2 = pack2(0.f, 0.f);
+#pragma unroll 4
     for (int v = tid; v < nvec; v += kSPThreads) {
       float x[T::VEC];
       unpack_vec<DT>(ld_shared_v4(sbase + v * 16), x);
 #pragma unroll
-      for (int k = 0; k < T::VEC; ++k) sum += ex2(fmaf(x[k], kLog2e, -mb));
+      for (int k = 0; k < T::VEC; k += 2) {
+        float t0, t1;
+        unpack2(fma2(pack2(x[k], x[k + 1]), k2, nmb2), t0, t1);
+        acc2 = add2(acc2, pack2(ex2(t0), ex2(t1)));
+      }
     }
+    float a0, a1;
+    unpack2(acc2, a0, a1);
+    sum = a0 + a1;
     if (tid < ntail) sum += ex2(fmaf(elem_at<DT>(sbase, nvec * T::VEC + tid), kLog2e, -mb));
   }
   const float sc = block_sum(sum, redf);
@@ -218,20 +257,35 @@ __global__ void __launch_bounds__(kSPThreads, 4) stats_probs_kernel(const __grid
       part_i = I;
     }
     cluster_sync();  // every CTA's partial is published
-    M = -INFINITY;
-    S = 0.f;
-    I = -1;
-    for (int k = 0; k < p.C; ++k) {
-      const float mk = ld_shared_cluster_f32(map_to_rank(smem_u32(&part_m), k));
-      M = fmaxf(M, mk);
+    if (tid < 32) {   // one warp reads the C partials (lane k: rank k) and merges in rank order
+      const int k = tid;
+      const bool has = k < p.C;
+      const float mk = has ? ld_shared_cluster_f32(map_to_rank(smem_u32(&part_m), k)) : -INFINITY;
+      const float sk = has ? ld_shared_cluster_f32(map_to_rank(smem_u32(&part_s), k)) : 0.f;
+      const int ik = has ? ld_shared_cluster_s32(map_to_rank(smem_u32(&part_i), k)) : -1;
+      float m = mk;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      float sum_all = 0.f;
+      int first = -1;
+      for (int j = 0; j < p.C; ++j) {  // rank order: the same sum in every CTA of the cluster
+        const float mj = __shfl_sync(kFull, mk, j);
+        const float sj = __shfl_sync(kFull, sk, j);
+        const int ij = __shfl_sync(kFull, ik, j);
+        if (mj == -INFINITY) continue;
+        sum_all += sj * ex2((mj - m) * kLog2e);
+        if (mj == m && first < 0) first = ij;
+      }
+      if (tid == 0) {
+        red_M = m;
+        red_S = sum_all;
+        red_I = first;
+      }
     }
-    for (int k = 0; k < p.C; ++k) {
-      const float mk = ld_shared_cluster_f32(map_to_rank(smem_u32(&part_m), k));
-      if (mk == -INFINITY) continue;
-      const float sk = ld_shared_cluster_f32(map_to_rank(smem_u32(&part_s), k));
-      S += sk * ex2((mk - M) * kLog2e);
-      if (mk == M && I < 0) I = ld_shared_cluster_s32(map_to_rank(smem_u32(&part_i), k));
-    }
+    __syncthreads();
+    M = red_M;
+    S = red_S;
+    I = red_I;
   }
   const float lse = M + logf(S);
   if (rank == 0 && tid == 0) {
@@ -245,31 +299,36 @@ __global__ void __launch_bounds__(kSPThreads, 4) stats_probs_kernel(const __grid
   const int vp = static_cast<int>(align_up(static_cast<size_t>(p.V), 64));
   const int e_end = min(vp, e0 + p.slabs_per_cta * 64);
   const float mb = lse * kLog2e;
-  for (int g = tid; e0 + g * 8 < e_end; g += kSPThreads) {
-    const int e = e0 + g * 8;  // 8 elements, one 16-byte store of P
+  const uint64_t k2 = pack2(kLog2e, kLog2e), nmb2 = pack2(-mb, -mb);
+  // P element (c, e) at ((e / 64) * R_pad + c) * 64 + e % 64: a 16-byte group g of this slice
+  // (8 elements) lands at slab (e0 / 64 + g / 8), byte (g % 8) * 16 of row c's 128-byte run
+  uint16_t* const prow = p.P + ((static_cast<int64_t>(e0 >> 6) * p.R_pad + c) << 6);
+  const int64_t slab_stride = static_cast<int64_t>(p.R_pad) << 6;  // elements between slabs
+  const int ngroups = (e_end - e0) / 8;
+#pragma unroll 4
+  for (int g = tid; g < ngroups; g += kSPThreads) {
+    const int e = e0 + g * 8;
     uint4 out = make_uint4(0u, 0u, 0u, 0u);
     if (ok && e < p.V) {
       float x[8];
       if constexpr (DT == DLLM_BF16) {
-        unpack_vec<DT>(ld_shared_v4(sbase + (e - e0) * 2), x);
+        unpack_vec<DT>(ld_shared_v4(sbase + g * 16), x);
       } else {
-        unpack_vec<DT>(ld_shared_v4(sbase + (e - e0) * 4), x);
-        unpack_vec<DT>(ld_shared_v4(sbase + (e - e0) * 4 + 16), x + 4);
+        unpack_vec<DT>(ld_shared_v4(sbase + g * 32), x);
+        unpack_vec<DT>(ld_shared_v4(sbase + g * 32 + 16), x + 4);
       }
       uint32_t w[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        const float lo = ex2(fmaf(x[2 * h], kLog2e, -mb));
-        const float hi = ex2(fmaf(x[2 * h + 1], kLog2e, -mb));
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[h]) : "f"(hi), "f"(lo));
+        float t0, t1;
+        unpack2(fma2(pack2(x[2 * h], x[2 * h + 1]), k2, nmb2), t0, t1);
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[h]) : "f"(ex2(t1)), "f"(ex2(t0)));
       }
       out = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    uint16_t* dst = p.P + ((static_cast<int64_t>(e >> 6) * p.R_pad + c) << 6) + (e & 63);
-    *reinterpret_cast<uint4*>(dst) = out;
+    *reinterpret_cast<uint4*>(prow + (g >> 3) * slab_stride + ((g & 7) << 3)) = out;
   }
   if (p.C > 1) cluster_sync();  // no CTA leaves while another may still read its partial
-  if (!ok) drain_bar(smem_u32(&bar), 0);  // a copy that outlived the wait lands before exit
 }
 
 }  // namespace
