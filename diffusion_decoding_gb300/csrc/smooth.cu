@@ -134,7 +134,7 @@ constexpr int kBM = 128;   // rows per CTA; a CTA pair covers 256
 constexpr int kBK = 64;    // one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;
 constexpr int kGemmThreads = 256;  // warp 0: TMEM allocation + MMA issue (leader);
-                                   // warps 1-7: TMA producers, one ring stage each;
+                                   // warps 1-7: producers, one ring stage each;
                                    // warps 4-7 then drain the accumulator (epilogue)
 constexpr int kProducers = 7;
 constexpr int kATileBytes = kBM * kBK * 2;
@@ -163,21 +163,19 @@ struct GemmParams {
 
 // One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
 // stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring.
-// Every stage has its own producer warp (seven of them): once the stage is free its lane 0
-// issues the stage's two TMA boxes in its CTA, and both CTAs' boxes complete on the leader CTA's "full" barrier for that stage (the leader's
-// producer posts the byte count of all four boxes).  The leader's MMA thread issues
-// tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each stage's release, and finally
-// the accumulator-ready signal, to both CTAs.  No thread relays progress across the pair (an
-// earlier version in which the peer's stages were forwarded by a cluster-scope release arrive
-// spent ~0.7 us per stage on that hop), and only lane 0 of a producer warp and one epilogue
-// thread poll barriers; the other epilogue threads wait at a hardware barrier.
+// Every stage has its own producer warp (seven of them): once the stage is free it issues the
+// stage's two TMA boxes in its CTA, and both CTAs' boxes complete on the leader CTA's "full"
+// barrier for that stage (the leader's producer posts the byte count of all four boxes).  The
+// leader's MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each
+// stage's release, and finally the accumulator-ready signal, to both CTAs.  No thread relays
+// progress across the pair: an earlier version in which the peer's stages were forwarded by a
+// cluster-scope release arrive spent ~0.7 us per stage on that hop.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     smooth_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t dyn_raw[];
   __shared__ uint64_t bars[2 * kMaxStages + 1];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int epi_ok;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -198,6 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int kb0 = ks * p.kb_per_split;
   const int nkb = max(0, min(p.num_kb, kb0 + p.kb_per_split) - kb0);
   const int S = p.stages;
+  const int P = min(S, kProducers);
   const uint32_t b_half_bytes = static_cast<uint32_t>(p.bn_max / 2) * kBK * 2;
 
   const uint32_t raw = smem_u32(dyn_raw);
@@ -228,30 +227,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_v = &abort_flag;
-  int last_k = -1;  // this producer's last issued K block (drained after an abort)
   const int prod = warp - 1;  // producer index of warps 1..7
-  const int P = min(S, kProducers);
+
+  int last_k = -1;  // this producer's last issued K block (drained after an abort)
   if (warp >= 1 && prod < P) {
-    // ---- producers (both CTAs): K blocks prod, prod + P, ... of own 128 P rows and own half of
-    // the E^T tile; lane 0 of each producer warp waits and issues.  (One thread issuing every
-    // stage delivered the operands ~20% slower: a thread's bulk copies do not all overlap.)
+    // ---- producers (both CTAs): K blocks prod, prod + P, ... of own 128 P rows and own half
+    // of the E^T tile; whole warps wait, lane 0 issues
+    const uint32_t leader_full0 = map_to_rank(full0, 0);
+    const uint32_t stage_tx = 2u * (kATileBytes + b_half_bytes);
     if (lane == 0) {
-      const uint32_t leader_full0 = map_to_rank(full0, 0);
-      const uint32_t stage_tx = 2u * (kATileBytes + b_half_bytes);
       prefetch_tensormap(&p.tmA);
       prefetch_tensormap(&p.tmB);
-      for (int k = prod; k < nkb; k += P) {
-        const int s = k % S;
-        const uint32_t ph = (k / S) & 1;
-        if (!wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status)) break;
+    }
+    for (int k = prod; k < nkb; k += P) {
+      const int s = k % S;
+      const uint32_t ph = (k / S) & 1;
+      if (!__all_sync(kFull, wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status))) break;
+      if (lane == 0) {
         const int slab = kb0 + k;
         if (leader) mbar_expect_tx(full0 + 8 * s, stage_tx);
         tma_load_slab_pair(sA + s * kATileBytes, &p.tmA, leader_full0 + 8 * s, my_m0, slab);
         tma_load_slab_pair(sB + s * b_half_bytes, &p.tmB, leader_full0 + 8 * s, my_n0, slab);
-        last_k = k;
       }
+      last_k = k;
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp == 0 && lane == 0 && leader) {
     // ---- MMA issuer (leader)
     const uint32_t idesc = idesc_bf16(2 * kBM, bn);
@@ -273,13 +273,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     umma_commit_pair(acc_bar);  // accumulators complete in both CTAs
   }
   if (warp >= 4) {
-    // ---- epilogue (both CTAs): this CTA's 128 accumulator rows, TMEM -> registers -> global.
-    // One thread waits for the accumulators; the four warps meet at a named barrier (no spin).
+    // ---- epilogue (both CTAs): this CTA's 128 accumulator rows, TMEM -> registers -> global
+    __syncwarp();
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int row = my_m0 + q * 32 + lane;
-    if (warp == 4 && lane == 0) epi_ok = wait_bar(acc_bar, 0, abort_v, p.status) ? 1 : 0;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    const bool ok = epi_ok != 0;  // warp-uniform: tcgen05.ld below is a .sync.aligned warp op
+    // warp-uniform: tcgen05.ld below is a .sync.aligned warp instruction
+    const bool ok = __all_sync(kFull, wait_bar(acc_bar, 0, abort_v, p.status));
     tc_fence_after();
     if (ok) {
       float* dst_base = p.split_k == 1
