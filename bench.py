@@ -165,6 +165,7 @@ _KERNEL_SOURCES = {
     "smooth_gemm_kernel": ["smooth.cu", "mbarrier.cuh"],
     "prob_rows_kernel": ["smooth.cu", "mbarrier.cuh"],
     "stats_partials_kernel": ["stats_commit.cu"],
+    "stats_probs_kernel": ["stats_probs.cu", "mbarrier.cuh"],
 }
 
 
