@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kScanThreads) compact_rows_kernel(const uint8_
                                                                     const int32_t* eos_hit,
                                                                     int B, int L, int32_t* row_ids,
                                                                     int32_t* M) {
+  pdl_wait();
+  pdl_trigger();
   const int R = B * L;
   int base = 0;
   for (int r0 = 0; r0 < R; r0 += kScanThreads) {
@@ -65,6 +67,8 @@ __global__ void __launch_bounds__(kScanThreads) read_rows_kernel(const uint8_t* 
                                                                  const int32_t* eos_hit, int B,
                                                                  int L, int32_t* rows,
                                                                  int32_t* count, dllm_stats st) {
+  pdl_wait();
+  pdl_trigger();
   const int R = B * L;
   int base = 0;
   for (int r0 = 0; r0 < R; r0 += kScanThreads) {
@@ -91,6 +95,8 @@ __global__ void __launch_bounds__(kScanThreads) read_rows_kernel(const uint8_t* 
 __global__ void __launch_bounds__(kScanThreads) kept_rows_map_kernel(
     const uint8_t* masked, const int32_t* eos_hit, int B, int L, int32_t* row_ids, int32_t* M,
     const int32_t* rows_read, const int32_t* count_read, int32_t* inv, int32_t* map) {
+  pdl_wait();
+  pdl_trigger();
   const int R = B * L;
   int base = 0;
   for (int r0 = 0; r0 < R; r0 += kScanThreads) {
@@ -117,6 +123,8 @@ __global__ void __launch_bounds__(kRefreshThreads) kv_refresh_kernel(const uint8
                                                                      int32_t* idx,
                                                                      int32_t* count) {
   extern __shared__ int cnt[];  // [L + 1]
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int T = P + L;
   const uint8_t* com = committed_now + static_cast<int64_t>(b) * L;
@@ -157,34 +165,30 @@ __global__ void __launch_bounds__(kRefreshThreads) kv_refresh_kernel(const uint8
 
 cudaError_t launch_compact_rows(const dllm_block_state& state, int B, int L, int32_t* row_ids,
                                 int32_t* M, cudaStream_t stream) {
-  compact_rows_kernel<<<1, kScanThreads, 0, stream>>>(state.masked, state.eos_hit, B, L, row_ids,
-                                                      M);
-  return cudaGetLastError();
+  return launch_dependent(compact_rows_kernel, dim3(1), dim3(kScanThreads), 0, stream,
+                          state.masked, state.eos_hit, B, L, row_ids, M);
 }
 
 cudaError_t launch_read_rows(const dllm_block_state& state, int B, int L, int32_t* rows,
                              int32_t* count, const dllm_stats& stats, cudaStream_t stream) {
-  read_rows_kernel<<<1, kScanThreads, 0, stream>>>(state.masked, state.eos_hit, B, L, rows, count,
-                                                   stats);
-  return cudaGetLastError();
+  return launch_dependent(read_rows_kernel, dim3(1), dim3(kScanThreads), 0, stream, state.masked,
+                          state.eos_hit, B, L, rows, count, stats);
 }
 
 cudaError_t launch_kept_rows_map(const dllm_block_state& state, int B, int L, int32_t* row_ids,
                                  int32_t* M, const int32_t* rows_read, const int32_t* count_read,
                                  int32_t* inv, int32_t* map, cudaStream_t stream) {
-  kept_rows_map_kernel<<<1, kScanThreads, 0, stream>>>(state.masked, state.eos_hit, B, L,
-                                                       row_ids, M, rows_read, count_read, inv,
-                                                       map);
-  return cudaGetLastError();
+  return launch_dependent(kept_rows_map_kernel, dim3(1), dim3(kScanThreads), 0, stream,
+                          state.masked, state.eos_hit, B, L, row_ids, M, rows_read, count_read,
+                          inv, map);
 }
 
 cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int prefix_len,
                               int window, uint8_t* refresh, int32_t* idx, int32_t* count,
                               cudaStream_t stream) {
   const size_t smem = sizeof(int) * (static_cast<size_t>(L) + 1);
-  kv_refresh_kernel<<<B, kRefreshThreads, smem, stream>>>(state.committed_now, L, prefix_len,
-                                                          window, refresh, idx, count);
-  return cudaGetLastError();
+  return launch_dependent(kv_refresh_kernel, dim3(B), dim3(kRefreshThreads), smem, stream,
+                          state.committed_now, L, prefix_len, window, refresh, idx, count);
 }
 
 }  // namespace dllm

@@ -186,6 +186,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int n_tile = tile % p.n_tiles;
   const int m_pair = tile / p.n_tiles;
   const int m0 = m_pair * 2 * kBM;
+  pdl_wait();  // P, M and the row map come from the kernels before this one
+  pdl_trigger();
   const int Mdev = *reinterpret_cast<const volatile int32_t*>(p.M);
   if (m0 >= Mdev) return;  // both CTAs of the pair leave together: no row of the pair is kept
 
@@ -324,6 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
 __global__ void splitk_reduce_kernel(const float* part, int split_k, int R_pad, int d,
                                      const int32_t* M, const int32_t* row_map, float* out) {
+  pdl_wait();
   const int Mdev = *M;
   const int d4 = d / 4;
   const size_t n4 = static_cast<size_t>(Mdev) * d4;
@@ -364,6 +367,8 @@ __global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* log
                                                                  int R_pad) {
   const int j = blockIdx.x / S;
   const int split = blockIdx.x - j * S;
+  pdl_wait();
+  pdl_trigger();
   if (j >= *M) return;
   const int r = row_ids[j];
   const float mb = lse[r] * kLog2e;
@@ -540,13 +545,12 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
   S = (Vp + chunk - 1) / chunk;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(R) * S));
   const int64_t rsb = sh.row_stride * es;
+  const char* lg = static_cast<const char*>(logits);
   if (sh.dtype == DLLM_BF16)
-    prob_rows_kernel<DLLM_BF16><<<grid, kProbThreads, 0, stream>>>(
-        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
-  else
-    prob_rows_kernel<DLLM_F32><<<grid, kProbThreads, 0, stream>>>(
-        static_cast<const char*>(logits), rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
-  return cudaGetLastError();
+    return launch_dependent(prob_rows_kernel<DLLM_BF16>, grid, dim3(kProbThreads), 0, stream, lg,
+                            rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
+  return launch_dependent(prob_rows_kernel<DLLM_F32>, grid, dim3(kProbThreads), 0, stream, lg,
+                          rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
 }
 
 cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const uint16_t* Et,
@@ -588,12 +592,12 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   if (e != cudaSuccess) return e;
   // m_tiles = 2 x row pairs: one CTA per 128 rows, clusters of 2 along x
   const dim3 grid(static_cast<unsigned>(pl.m_tiles * pl.n_tiles * pl.split_k));
-  smooth_gemm_kernel<<<grid, kGemmThreads, smem, stream>>>(gp);
-  e = cudaGetLastError();
+  e = launch_dependent(smooth_gemm_kernel, grid, dim3(kGemmThreads), smem, stream, gp);
   if (e != cudaSuccess || pl.split_k == 1) return e;
-  splitk_reduce_kernel<<<std::min(1024, std::max(1, pl.R * pl.d / 4 / 256)), 256, 0, stream>>>(
-      gp.part, pl.split_k, R_pad, pl.d, M, row_map, out);
-  return cudaGetLastError();
+  return launch_dependent(splitk_reduce_kernel,
+                          dim3(std::min(1024, std::max(1, pl.R * pl.d / 4 / 256))), dim3(256), 0,
+                          stream, static_cast<const float*>(gp.part), pl.split_k, R_pad, pl.d, M,
+                          row_map, out);
 }
 
 cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns,

@@ -546,10 +546,11 @@ __device__ __forceinline__ void write_row_stats(const dllm_stats& st, int64_t r,
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams p) {
+  // the block state comes from the kernel before this one (the previous step's commit)
+  pdl_wait();
   // let the commit kernel's CTAs become resident while this grid's last waves run (earlier
   // CTAs count as triggered when they exit, so its CTAs do not hold SMs for the whole pass)
-  if (static_cast<int>(blockIdx.x) >= p.pdl_from)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (static_cast<int>(blockIdx.x) >= p.pdl_from) pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp;
   const int S = p.S, L = p.c.L;
@@ -660,7 +661,8 @@ __global__ void __launch_bounds__(kCommitThreads) commit_only_kernel(CommitOnlyP
   extern __shared__ __align__(1024) uint8_t dyn[];
   // launched after the statistics kernel as a programmatic dependent launch (or plainly):
   // wait until every partial, statistic and read of the block state there is complete
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   const int L = p.c.L;
   const int b = blockIdx.x;
@@ -701,6 +703,8 @@ struct ShardParams {
 };
 
 __global__ void __launch_bounds__(256) merge_shards_kernel(const __grid_constant__ ShardParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (r >= p.rows) return;
   float m = -INFINITY;
@@ -786,11 +790,10 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   const int64_t items = static_cast<int64_t>(R) * p.S;
   const dim3 grid1(static_cast<unsigned>((items + kThreads / 32 - 1) / (kThreads / 32)));
   p.pdl_from = std::max(0, static_cast<int>(grid1.x) - 2 * 4 * std::max(1, sm_count));
-  if (sh.dtype == DLLM_BF16)
-    stats_partials_kernel<DLLM_BF16><<<grid1, kThreads, 0, stream>>>(p);
-  else
-    stats_partials_kernel<DLLM_F32><<<grid1, kThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e =
+      sh.dtype == DLLM_BF16
+          ? launch_dependent(stats_partials_kernel<DLLM_BF16>, grid1, dim3(kThreads), 0, stream, p)
+          : launch_dependent(stats_partials_kernel<DLLM_F32>, grid1, dim3(kThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
   if (ca.mode == kStatsOnly && p.S == 1) return cudaSuccess;
   // the merge (+ commit) kernel, one CTA per sequence, as a programmatic dependent launch
@@ -822,8 +825,8 @@ cudaError_t launch_merge_shard_stats(const dllm_shard_stats* shards, int n, int6
   p.n = n;
   p.rows = rows;
   p.out = out;
-  merge_shards_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(merge_shards_kernel, dim3(static_cast<unsigned>((rows + 255) / 256)),
+                          dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,
@@ -836,8 +839,8 @@ cudaError_t launch_commit_only(const dllm_shape& sh, const dllm_stats& stats,
   p.c.state = state;
   p.c.ca = ca;
   p.S = 1;  // statistics already complete: commit only
-  commit_only_kernel<<<sh.B, kCommitThreads, epi_smem_bytes(sh.L), stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(commit_only_kernel, dim3(sh.B), dim3(kCommitThreads),
+                          epi_smem_bytes(sh.L), stream, p);
 }
 
 }  // namespace dllm

@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(kSPThreads, 3) stats_probs_kernel(const __grid
   const uint32_t rank = p.C > 1 ? cluster_ctarank() : 0u;
   const int cl = static_cast<int>(blockIdx.x) / p.C;  // this cluster, the same in all its CTAs
   const int n_cl = static_cast<int>(gridDim.x) / p.C;
+  pdl_wait();  // the row list comes from the kernel before this one
+  pdl_trigger();
   const int count = *reinterpret_cast<const volatile int32_t*>(p.count);
   const int e0 = static_cast<int>(rank) * p.slabs_per_cta * 64;
   const int n = max(0, min(p.V, e0 + p.slabs_per_cta * 64) - e0);  // elements of this slice
@@ -417,13 +419,15 @@ cudaError_t launch_stats_probs(const void* logits, const dllm_shape& sh, const i
   cfg.blockDim = dim3(kSPThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // persistent: as many clusters as can be resident at once, no more than there are rows
   const int n_cl = resident_clusters(reinterpret_cast<const void*>(kern), cfg, sh.dtype, p.C, smem);
   cfg.gridDim = dim3(static_cast<unsigned>(p.C * std::min(n_cl, sh.B * sh.L)));
