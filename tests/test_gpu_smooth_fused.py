@@ -15,12 +15,15 @@ import diffusion_decoding_gb300 as dd
 pytestmark = pytest.mark.gpu
 
 
-def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None):
+def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None):
     gpu = GpuDecoder(w)
     ost = oracle.BlockState(w.B, w.L)
     if masked0 is not None:
         ost.masked[:] = masked0
         gpu.state.masked.copy_(torch.from_numpy(masked0.reshape(-1)).cuda())
+    if eos0 is not None:  # sequences already stopped: nothing of theirs is read or smoothed
+        ost.eos_hit[:] = eos0
+        gpu.state.eos_hit.copy_(torch.from_numpy(eos0.astype(np.int32)).cuda())
     lg, _, s = guarded_logits(w, seed, 0, ost, calibrated)
     s_ref, _ = oracle_step(w, ost, lg, s)
     E, Et = _table(w.V, w.d)
@@ -81,3 +84,10 @@ def test_fused_full_size_sampled_rows():
     w = synth.WORKLOADS["smooth_step"]
     Mg = _fused_case(w, synth.workloads.SEEDS[w.key], calibrated=False, sample_rows=6)
     assert Mg == w.B * w.L - w.B
+
+
+def test_fused_with_a_stopped_sequence():
+    w = synth.WORKLOADS["smooth_step"].scaled(B=3, L=32, V=20000, d=128, prefix_len=8)
+    eos0 = np.array([0, 1, 0], np.int32)
+    Mg = _fused_case(w, seed=9, calibrated=True, eos0=eos0)
+    assert 0 < Mg < 2 * w.L
