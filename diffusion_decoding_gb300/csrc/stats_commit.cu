@@ -10,7 +10,7 @@
 //    waited behind the loads in flight.)
 // 2. commit_only_kernel (one CTA per sequence, chained with programmatic dependent launch so it
 //    is resident before the first kernel drains): merges the slice partials of its sequence's
-//    rows into their statistics (four threads per row, every load issued up front), then runs
+//    rows into their statistics (eight threads per row, every load issued up front), then runs
 //    the commit decision in shared memory (threshold, hierarchical or credit decoding; dInfer
 //    explainer, decoding-strategy component, methods 1-3).  In statistics-only mode it only
 //    merges.

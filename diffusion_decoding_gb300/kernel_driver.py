@@ -1,13 +1,14 @@
 """Run one kernel family of the decode step a fixed number of times, for external profilers.
 
-    python -m diffusion_decoding_gb300.kernel_driver {stats|probs|gemm|step|fused} [n]
+    python -m diffusion_decoding_gb300.kernel_driver {stats|probs|gemm|step|fused} [n [B L]]
 
 The inputs have the smoothing-step sizes (B=16, L=64, V=126464 bf16 logits, d=2048 embedding
-table; about 0.8 GB on the device), so every launch reads more than the L2 holds.  Nothing is
-timed here: a profiler (ncu) attaches to the launches.  `stats` runs the fused statistics +
-threshold commit; `probs` the probability rows; `gemm` the smoothing GEMM (after one
-probability pass); `step` the whole step (commit, probabilities, GEMM, KV refresh) through the
-separate calls; `fused` the whole step through the single-read call.
+table; about 0.8 GB on the device), so every launch reads more than the L2 holds; `stats`
+takes another block shape as B and L (every position masked, as in a loop's first
+iteration).  Nothing is timed here: a profiler (ncu) attaches to the launches.  `stats` runs
+the fused statistics + threshold commit; `probs` the probability rows; `gemm` the smoothing
+GEMM (after one probability pass); `step` the whole step (commit, probabilities, GEMM, KV
+refresh) through the separate calls; `fused` the whole step through the single-read call.
 """
 import sys
 
@@ -15,7 +16,7 @@ import torch
 
 import diffusion_decoding_gb300 as dd
 
-B, L, V, D = 16, 64, 126464, 2048
+B_, L_, V, D = 16, 64, 126464, 2048
 PREFIX, WINDOW, TAU = 1024, 4, 0.9
 
 
@@ -24,6 +25,7 @@ def main(argv) -> None:
     n = int(argv[1]) if len(argv) > 1 else 4
     if what not in ("stats", "probs", "gemm", "step", "fused"):
         raise SystemExit(f"unknown kernel family {what!r}")
+    B, L = (int(argv[2]), int(argv[3])) if what == "stats" and len(argv) > 3 else (B_, L_)
     dev = torch.device("cuda")
     g = torch.Generator(device=dev)
     g.manual_seed(7)
