@@ -92,6 +92,7 @@ struct SmoothPlan {
   int bn_max;     // widest column tile (multiple of 16, <= 256)
   int split_k;    // >1: partial sums reduced by a second kernel
   int stages;     // TMA/MMA pipeline depth
+  int slabs_per_stage;  // 64-wide K slabs per ring stage (one TMA box of that depth per operand)
   size_t ws_bytes;
   size_t off_p;       // bf16 P, K-slab-blocked [ldp / 64][R_pad][64]
   size_t off_part;    // fp32 partials [split_k, R_pad, d]

@@ -141,8 +141,8 @@ constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kMaxStages = 8;
 
 struct GemmParams {
-  CUtensorMap tmA;    // P: K-slab-blocked [slabs][R_pad][64], boxes of 64 x 128 x 1
-  CUtensorMap tmB;    // E^T: K-slab-blocked [slabs][d][64], boxes of 64 x bn_max/2 x 1
+  CUtensorMap tmA;    // P: K-slab-blocked [slabs][R_pad][64], boxes of 64 x 128 x gs
+  CUtensorMap tmB;    // E^T: K-slab-blocked [slabs][d][64], boxes of 64 x bn_max/2 x gs
   int num_kb;         // 64-wide K blocks over V
   int n_tiles;
   int bn_base;        // narrow pair-tile width; the first bn_rem tiles are 16 wider
@@ -151,6 +151,7 @@ struct GemmParams {
   int split_k;
   int kb_per_split;
   int stages;
+  int gs;             // K slabs per stage
   int tmem_cols;
   int d;
   int R_pad;
@@ -162,7 +163,8 @@ struct GemmParams {
 };
 
 // One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
-// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring.
+// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring
+// whose stages hold `gs` consecutive 64-wide K slabs of each operand (one TMA box each).
 // Every stage has its own producer warp (seven of them): once the stage is free it issues the
 // stage's two TMA boxes in its CTA, and both CTAs' boxes complete on the leader CTA's "full"
 // barrier for that stage (the leader's producer posts the byte count of all four boxes).  The
@@ -199,12 +201,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int nkb = max(0, min(p.num_kb, kb0 + p.kb_per_split) - kb0);
   const int S = p.stages;
   const int P = min(S, kProducers);
+  const int G = p.gs;
+  const int nst = (nkb + G - 1) / G;  // ring stages this pair consumes
   const uint32_t b_half_bytes = static_cast<uint32_t>(p.bn_max / 2) * kBK * 2;
+  const uint32_t a_stage = static_cast<uint32_t>(G) * kATileBytes;
+  const uint32_t b_stage = static_cast<uint32_t>(G) * b_half_bytes;
 
   const uint32_t raw = smem_u32(dyn_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   const uint32_t sA = sbase;
-  const uint32_t sB = sbase + S * kATileBytes;
+  const uint32_t sB = sbase + S * a_stage;
   const uint32_t full0 = smem_u32(&bars[0]);
   const uint32_t empty0 = smem_u32(&bars[kMaxStages]);
   const uint32_t acc_bar = smem_u32(&bars[2 * kMaxStages]);
@@ -231,25 +237,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_v = &abort_flag;
   const int prod = warp - 1;  // producer index of warps 1..7
 
-  int last_k = -1;  // this producer's last issued K block (drained after an abort)
+  int last_k = -1;  // this producer's last issued stage (drained after an abort)
   if (warp >= 1 && prod < P) {
-    // ---- producers (both CTAs): K blocks prod, prod + P, ... of own 128 P rows and own half
-    // of the E^T tile; whole warps wait, lane 0 issues
+    // ---- producers (both CTAs): stages prod, prod + P, ... of own 128 P rows and own half
+    // of the E^T tile; whole warps wait, lane 0 issues.  A box reaching past the last slab
+    // reads zeros there and still counts its full size.
     const uint32_t leader_full0 = map_to_rank(full0, 0);
-    const uint32_t stage_tx = 2u * (kATileBytes + b_half_bytes);
+    const uint32_t stage_tx = 2u * (a_stage + b_stage);
     if (lane == 0) {
       prefetch_tensormap(&p.tmA);
       prefetch_tensormap(&p.tmB);
     }
-    for (int k = prod; k < nkb; k += P) {
+    for (int k = prod; k < nst; k += P) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
       if (!__all_sync(kFull, wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status))) break;
       if (lane == 0) {
-        const int slab = kb0 + k;
+        const int slab = kb0 + k * G;
         if (leader) mbar_expect_tx(full0 + 8 * s, stage_tx);
-        tma_load_slab_pair(sA + s * kATileBytes, &p.tmA, leader_full0 + 8 * s, my_m0, slab);
-        tma_load_slab_pair(sB + s * b_half_bytes, &p.tmB, leader_full0 + 8 * s, my_n0, slab);
+        tma_load_slab_pair(sA + s * a_stage, &p.tmA, leader_full0 + 8 * s, my_m0, slab);
+        tma_load_slab_pair(sB + s * b_stage, &p.tmB, leader_full0 + 8 * s, my_n0, slab);
       }
       last_k = k;
       __syncwarp();
@@ -257,18 +264,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 0 && lane == 0 && leader) {
     // ---- MMA issuer (leader)
     const uint32_t idesc = idesc_bf16(2 * kBM, bn);
-    int k = 0;
-    for (; k < nkb; ++k) {
+    for (int k = 0; k < nst; ++k) {
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
       if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
       tc_fence_after();
-      const uint32_t a_s = sA + s * kATileBytes;
-      const uint32_t b_s = sB + s * b_half_bytes;
+      const int nv = min(G, nkb - k * G);  // slabs of this stage inside the pair's K range
+      for (int g = 0; g < nv; ++g) {
+        const uint32_t a_s = sA + s * a_stage + g * kATileBytes;
+        const uint32_t b_s = sB + s * b_stage + g * b_half_bytes;
 #pragma unroll
-      for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-        umma_bf16_pair(tmem, sw128_desc(a_s + kk * kUmmaK * 2), sw128_desc(b_s + kk * kUmmaK * 2),
-                       idesc, (k > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+          umma_bf16_pair(tmem, sw128_desc(a_s + kk * kUmmaK * 2),
+                         sw128_desc(b_s + kk * kUmmaK * 2), idesc,
+                         (k > 0 || g > 0 || kk > 0) ? 1u : 0u);
+        }
       }
       umma_commit_pair(empty0 + 8 * s);  // stage s is free in both CTAs once these MMAs read it
     }
@@ -454,16 +464,17 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// K-slab-blocked bf16 operand [slabs][rows][64] as a 3-D tensor map; boxes of 64 x box_rows x 1
-// with 128-byte swizzle (the K-major layout the tcgen05 descriptors expect).  Rows of a box
-// beyond `rows` read as zeros.
+// K-slab-blocked bf16 operand [slabs][rows][64] as a 3-D tensor map; boxes of
+// 64 x box_rows x box_slabs with 128-byte swizzle (the K-major layout the tcgen05 descriptors
+// expect; the slabs of a box land one after another in shared memory).  Rows or slabs of a box
+// beyond the tensor read as zeros.
 bool make_slab_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t slabs,
-                   uint32_t box_rows) {
+                   uint32_t box_rows, uint32_t box_slabs) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {64, rows, slabs};
   cuuint64_t strides[2] = {128, rows * 128};
-  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t box[3] = {64, box_rows, box_slabs};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -506,7 +517,11 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
       }
     }
   }
-  const size_t stage_bytes = kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2;
+  // Two slabs per stage halve the stage hand-offs per MMA (three stages fit); one slab when
+  // two would leave fewer than three stages.
+  const size_t slab_bytes = kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2;
+  pl.slabs_per_stage = (kMaxDynSmem - 2048) / (2 * slab_bytes) >= 3 ? 2 : 1;
+  const size_t stage_bytes = pl.slabs_per_stage * slab_bytes;
   pl.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage_bytes));
   pl.stages = std::min(pl.stages, kProducers);  // one producer warp per stage
   const int R_pad = pl.m_tiles * kBM;
@@ -560,8 +575,9 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   (void)ldt;
   GemmParams gp{};
   const uint64_t slabs = static_cast<uint64_t>(pl.ldp) / 64;
-  if (!make_slab_map(&gp.tmA, P, R_pad, slabs, kBM) ||
-      !make_slab_map(&gp.tmB, Et, pl.d, slabs, pl.bn_max / 2)) {
+  const int G = std::max(1, pl.slabs_per_stage);
+  if (!make_slab_map(&gp.tmA, P, R_pad, slabs, kBM, G) ||
+      !make_slab_map(&gp.tmB, Et, pl.d, slabs, pl.bn_max / 2, G)) {
     *why = "cuTensorMapEncodeTiled failed or is unavailable (E^T must be 16-byte aligned)";
     return cudaErrorInvalidValue;
   }
@@ -574,6 +590,7 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.split_k = pl.split_k;
   gp.kb_per_split = (gp.num_kb + pl.split_k - 1) / pl.split_k;
   gp.stages = pl.stages;
+  gp.gs = G;
   int cols = 32;
   while (cols < pl.bn_max) cols *= 2;
   gp.tmem_cols = cols;
@@ -584,7 +601,7 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.M = M;
   gp.row_map = row_map;
   gp.status = static_cast<int32_t*>(ws);
-  const size_t smem = static_cast<size_t>(pl.stages) *
+  const size_t smem = static_cast<size_t>(pl.stages) * G *
                           (kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2) + 1024;
   cudaError_t e = cudaFuncSetAttribute(smooth_gemm_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
