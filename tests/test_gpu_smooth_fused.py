@@ -15,7 +15,8 @@ import diffusion_decoding_gb300 as dd
 pytestmark = pytest.mark.gpu
 
 
-def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None):
+def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None,
+                padded=False):
     gpu = GpuDecoder(w)
     ost = oracle.BlockState(w.B, w.L)
     if masked0 is not None:
@@ -33,7 +34,13 @@ def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None):
     M = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
     dt = dd.DLLM_BF16 if w.dtype == "bf16" else dd.DLLM_F32
-    dd.dllm_commit_threshold_smooth(to_device(lg), gpu.shape, gpu.stats, gpu.state, w.tau,
+    shape, lgd = gpu.shape, lg
+    if padded:  # rows padded by 8 elements holding huge values that must never be read
+        stride = w.V + 8
+        lgd = np.full((w.B, w.L, stride), 0x7F7F if w.dtype == "bf16" else 3e38, lg.dtype)
+        lgd[:, :, :w.V] = lg
+        shape = dd.make_shape(w.B, w.L, w.V, dt, row_stride=stride)
+    dd.dllm_commit_threshold_smooth(to_device(lgd), shape, gpu.stats, gpu.state, w.tau,
                                     w.eos_id, Et, w.d, out, row_ids, M, ws)
     torch.cuda.synchronize()
     assert dd.dllm_get_status(ws) == dd.DLLM_OK
@@ -70,6 +77,17 @@ def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None):
 def test_fused_small_all_rows(B, L, V, d):
     w = synth.WORKLOADS["smooth_step"].scaled(B=B, L=L, V=V, d=d, prefix_len=16)
     assert _fused_case(w, seed=B * 1000 + V, calibrated=True) > 0
+
+
+@pytest.mark.parametrize("V,dtype", [
+    (1000, "bf16"),    # one CTA per row, a partial last 64-element slab
+    (20008, "bf16"),   # clusters of 2, the second CTA's slice ends inside a slab
+    (8200, "f32"),     # clusters of 2 over fp32 rows
+    (8, "f32"),        # a row of two vectors (smoothing needs V a multiple of 8)
+])
+def test_fused_ragged_vocab_padded_stride(V, dtype):
+    w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=40, V=V, d=48, prefix_len=4, dtype=dtype)
+    assert _fused_case(w, seed=V, calibrated=V > 16, padded=True) > 0
 
 
 def test_fused_partial_mask_and_fp32():
