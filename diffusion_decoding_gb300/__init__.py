@@ -92,6 +92,8 @@ _SIGS = {
                                    _c_sz, _c_vp]),
     "dllm_smooth_gemm": (_c_i32, [ctypes.POINTER(dllm_shape), _c_vp, _c_i32, _c_vp, _c_vp, _c_vp,
                                   _c_sz, _c_vp]),
+    "dllm_block_state_reset": (_c_i32, [ctypes.POINTER(dllm_block_state), _c_i32, _c_i32, _c_vp,
+                                        _c_vp, _c_i32, _c_vp]),
     "dllm_kv_refresh_mask": (_c_i32, [ctypes.POINTER(dllm_block_state), _c_i32, _c_i32, _c_i32,
                                       _c_i32, _c_vp, _c_vp, _c_vp, _c_vp]),
     "dllm_get_status": (_c_i32, [_c_vp, _c_vp, ctypes.POINTER(_c_i32)]),
@@ -193,14 +195,9 @@ class BlockState:
         return dllm_block_state(_ptr(self.masked), _ptr(self.tokens), _ptr(self.committed_now),
                                 _ptr(self.n_commit), _ptr(self.eos_hit))
 
-    def reset(self) -> None:
-        self.masked.fill_(1)
-        self.tokens.fill_(-1)
-        self.committed_now.zero_()
-        self.n_commit.zero_()
-        self.eos_hit.zero_()
-        self.cand_id.fill_(-1)
-        self.cand_credit.zero_()
+    def reset(self, stream=None) -> None:
+        """A new block, by one kernel (dllm_block_state_reset), credit slots included."""
+        dllm_block_state_reset(self, stream=stream)
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:
@@ -326,6 +323,16 @@ def dllm_smooth_gemm(shape, Et, d: int, out, M, ws, stream=None) -> None:
     _check(lib().dllm_smooth_gemm(ctypes.byref(shape), _ptr(Et), d, _ptr(out), _ptr(M), _ptr(ws),
                                   ws.numel(), _stream(stream)),
            "dllm_smooth_gemm")
+
+
+def dllm_block_state_reset(state: BlockState, credit: bool = True, stream=None) -> None:
+    bs = state.c()
+    K = state.cand_id.shape[1]
+    _check(lib().dllm_block_state_reset(ctypes.byref(bs), state.B, state.L,
+                                        _ptr(state.cand_id) if credit else None,
+                                        _ptr(state.cand_credit) if credit else None,
+                                        K if credit else 0, _stream(stream)),
+           "dllm_block_state_reset")
 
 
 def dllm_kv_refresh_mask(state: BlockState, prefix_len: int, window: int, refresh, idx, count,

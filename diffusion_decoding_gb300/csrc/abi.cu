@@ -386,6 +386,27 @@ dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* s
   return ok();
 }
 
+dllm_status dllm_block_state_reset(const dllm_block_state* state, int32_t B, int32_t L,
+                                   int32_t* cand_id, float* cand_credit, int32_t K,
+                                   dllm_stream_t stream) {
+  DLLM_TRY(check_state(state));
+  if (B < 1 || L < 1) return fail(DLLM_ERR_INVALID_ARG, "need B, L >= 1 (B=%d L=%d)", B, L);
+  if (L > dllm::kMaxL) return fail(DLLM_ERR_UNSUPPORTED, "L=%d exceeds %d", L, dllm::kMaxL);
+  if (static_cast<int64_t>(B) * L > (int64_t{1} << 20))
+    return fail(DLLM_ERR_UNSUPPORTED, "B*L=%lld exceeds 2^20",
+                static_cast<long long>(B) * L);
+  const bool credit = cand_id != nullptr || cand_credit != nullptr;
+  if (credit && (K < 1 || K > dllm::kMaxK))
+    return fail(DLLM_ERR_INVALID_ARG, "K=%d must be in [1, %d] with credit slots", K,
+                dllm::kMaxK);
+  const int64_t n = static_cast<int64_t>(B) * L;
+  cudaError_t e = dllm::launch_block_state_reset(*state, n, B, cand_id, cand_credit,
+                                                 credit ? n * K : 0,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_block_state_reset");
+  return ok();
+}
+
 dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32_t L,
                                  int32_t prefix_len, int32_t window, uint8_t* refresh,
                                  int32_t* idx, int32_t* count, dllm_stream_t stream) {

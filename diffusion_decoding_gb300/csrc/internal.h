@@ -77,6 +77,11 @@ cudaError_t launch_kept_rows_map(const dllm_block_state& state, int B, int L, in
                                  int32_t* M, const int32_t* rows_read, const int32_t* count_read,
                                  int32_t* inv, int32_t* map, cudaStream_t stream);
 
+// Fresh block state (every position masked); the credit slots too when given (nk > 0).
+cudaError_t launch_block_state_reset(const dllm_block_state& state, int64_t n, int B,
+                                     int32_t* cand_id, float* cand_credit, int64_t nk,
+                                     cudaStream_t stream);
+
 cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int prefix_len,
                               int window, uint8_t* refresh, int32_t* idx, int32_t* count,
                               cudaStream_t stream);

@@ -3,6 +3,8 @@
 //
 // Both are tiny (at most B*L flags, or P + L cache positions per sequence) and latency-bound; they
 // use warp ballots and shuffle prefix sums, never a global barrier.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -181,6 +183,42 @@ cudaError_t launch_kept_rows_map(const dllm_block_state& state, int B, int L, in
   return launch_dependent(kept_rows_map_kernel, dim3(1), dim3(kScanThreads), 0, stream,
                           state.masked, state.eos_hit, B, L, row_ids, M, rows_read, count_read,
                           inv, map);
+}
+
+// A new block: n = B*L positions masked with no token and nothing committed this step, B
+// sequences with no commit counted and no stop; nk = B*L*K credit slots empty with zero credit.
+__global__ void __launch_bounds__(256) block_state_reset_kernel(dllm_block_state st, int64_t n,
+                                                                int B, int32_t* cand_id,
+                                                                float* cand_credit, int64_t nk) {
+  pdl_wait();  // the calls before this one may still read the state
+  pdl_trigger();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t end = max(n, nk);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < end;
+       i += stride) {
+    if (i < n) {
+      st.masked[i] = 1;
+      st.tokens[i] = -1;
+      st.committed_now[i] = 0;
+    }
+    if (i < B) {
+      st.n_commit[i] = 0;
+      st.eos_hit[i] = 0;
+    }
+    if (i < nk) {
+      if (cand_id != nullptr) cand_id[i] = -1;
+      if (cand_credit != nullptr) cand_credit[i] = 0.f;
+    }
+  }
+}
+
+cudaError_t launch_block_state_reset(const dllm_block_state& state, int64_t n, int B,
+                                     int32_t* cand_id, float* cand_credit, int64_t nk,
+                                     cudaStream_t stream) {
+  const int64_t end = std::max(n, nk);
+  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(1024, (end + 255) / 256));
+  return launch_dependent(block_state_reset_kernel, dim3(std::max(1u, blocks)), dim3(256), 0,
+                          stream, state, n, B, cand_id, cand_credit, nk);
 }
 
 cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int prefix_len,

@@ -103,6 +103,19 @@ typedef struct {
 /* Description of the last error on this thread ("" if none). */
 const char* dllm_last_error(void);
 
+/*
+ * Start a new block (dInfer explainer, diffusion-iteration manager: a block starts with every
+ * position masked and is decoded over iterations until filled or stopped): one kernel sets
+ *   masked[B*L] = 1, tokens[B*L] = -1, committed_now[B*L] = 0, n_commit[B] = 0, eos_hit[B] = 0
+ * and, when cand_id / cand_credit are not NULL (the credit-decoding state, [B*L, K] each),
+ * cand_id = -1 (empty slot) and cand_credit = 0.  1 <= K <= 16 when either is given.
+ * B >= 1, 1 <= L <= 1024, B*L <= 2^20.  Same stream rules as every call: it is ordered after
+ * the calls before it on `stream`, so a decode loop with its reset can be captured whole.
+ */
+dllm_status dllm_block_state_reset(const dllm_block_state* state, int32_t B, int32_t L,
+                                   int32_t* cand_id, float* cand_credit, int32_t K,
+                                   dllm_stream_t stream);
+
 /* Bytes of workspace the stats and commit calls need for `shape` (0 if shape is invalid). */
 size_t dllm_workspace_bytes(const dllm_shape* shape);
 

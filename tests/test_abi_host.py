@@ -81,6 +81,14 @@ def test_pointer_validation(lib):
         == dd.DLLM_ERR_INVALID_ARG
     assert lib.dllm_kv_refresh_mask(ctypes.byref(bs), 2, 8, -1, 4, 16, 16, 16, None) \
         == dd.DLLM_ERR_INVALID_ARG
+    assert lib.dllm_block_state_reset(ctypes.byref(bad), 2, 8, None, None, 0, None) \
+        == dd.DLLM_ERR_INVALID_ARG  # a null state array
+    assert lib.dllm_block_state_reset(ctypes.byref(bs), 0, 8, None, None, 0, None) \
+        == dd.DLLM_ERR_INVALID_ARG
+    assert lib.dllm_block_state_reset(ctypes.byref(bs), 2, 1025, None, None, 0, None) \
+        == dd.DLLM_ERR_UNSUPPORTED
+    assert lib.dllm_block_state_reset(ctypes.byref(bs), 2, 8, 16, 16, 17, None) \
+        == dd.DLLM_ERR_INVALID_ARG  # K beyond the slot limit
     assert lib.dllm_kv_refresh_mask(ctypes.byref(bs), 2, 8, 65530, 4, 16, 16, 16, None) \
         == dd.DLLM_ERR_UNSUPPORTED
     assert lib.dllm_prepare_embedding(16, 100, 24, 16, None) == dd.DLLM_ERR_UNSUPPORTED

@@ -34,6 +34,36 @@ def test_credit_state_checkpoint_resume_is_bit_identical():
         assert np.array_equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("B,L,K", [(1, 1, 1), (3, 100, 8), (64, 1024, 16)])
+def test_block_state_reset_gives_a_fresh_block(B, L, K):
+    # every array scribbled over, then one reset: the oracle's fresh state, exactly
+    import oracle
+    st = dd.BlockState(B, L, K)
+    g = torch.Generator(device="cuda").manual_seed(B * L + K)
+    for t in (st.masked, st.committed_now):
+        t.copy_(torch.randint(0, 256, t.shape, generator=g, device="cuda").to(t.dtype))
+    for t in (st.tokens, st.n_commit, st.eos_hit, st.cand_id):
+        t.copy_(torch.randint(-9, 99999, t.shape, generator=g, device="cuda").to(t.dtype))
+    st.cand_credit.uniform_(0.0, 3.0, generator=g)
+    st.reset()
+    ref = oracle.BlockState(B, L, K)
+    for k in ("masked", "tokens", "committed_now", "n_commit", "eos_hit", "cand_id"):
+        assert np.array_equal(getattr(st, k).cpu().numpy().reshape(getattr(ref, k).shape),
+                              getattr(ref, k)), k
+    assert np.array_equal(st.cand_credit.cpu().numpy().reshape(ref.cand_credit.shape),
+                          ref.cand_credit.astype(np.float32))
+
+
+def test_block_state_reset_without_credit_slots_leaves_them():
+    st = dd.BlockState(2, 16, 8)
+    st.cand_id.fill_(7)
+    st.cand_credit.fill_(1.5)
+    st.masked.zero_()
+    dd.dllm_block_state_reset(st, credit=False)
+    assert bool((st.masked == 1).all()) and bool((st.cand_id == 7).all())
+    assert bool((st.cand_credit == 1.5).all())
+
+
 def _smooth_setup(w, seed=9):
     gpu = GpuDecoder(w)
     E = synth.embedding_table(seed, w.V, w.d)
