@@ -317,7 +317,7 @@ dllm_status dllm_smooth_gemm(const dllm_shape* shape, const uint16_t* Et, int32_
       reinterpret_cast<const uint16_t*>(static_cast<const char*>(ws) + pl.off_p);
   const char* why = "launch failed";
   const int ldt = static_cast<int>(dllm::align_up(static_cast<size_t>(shape->V), 8));
-  cudaError_t e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, M, nullptr, ws,
+  cudaError_t e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, M, nullptr, false, ws,
                                            reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess)
     return fail(DLLM_ERR_CUDA, "dllm_smooth_gemm: %s: %s", why, cudaGetErrorString(e));
@@ -379,7 +379,9 @@ dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* s
   if (e != cudaSuccess) return cuda_fail(e, "dllm_commit_threshold_smooth (commit)");
   const char* why = "launch failed";
   const int ldt = static_cast<int>(dllm::align_up(static_cast<size_t>(shape->V), 8));
-  e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, count, map, ws, st, &why);
+  // P (statistics kernel) and count (row list) predate the kept-row map, the only input the
+  // kernel just before the GEMM writes: the GEMM's mainloop overlaps it
+  e = dllm::launch_smooth_gemm(pl, P, Et, ldt, out, count, map, true, ws, st, &why);
   if (e != cudaSuccess)
     return fail(DLLM_ERR_CUDA, "dllm_commit_threshold_smooth: %s: %s", why,
                 cudaGetErrorString(e));

@@ -114,9 +114,11 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
                              int sm_count, cudaStream_t stream);
 
 // out row of P row j: row_map[j] (-1: not written) when row_map is not null, else j.
+// wait_late: P and M were written before the kernel launched just before this one, which only
+// writes row_map (the single-read step): the GEMM's mainloop may overlap that kernel.
 cudaError_t launch_smooth_gemm(const SmoothPlan& plan, const uint16_t* P, const uint16_t* Et,
                                int ldt, float* out, const int32_t* M, const int32_t* row_map,
-                               void* ws, cudaStream_t stream, const char** why);
+                               bool wait_late, void* ws, cudaStream_t stream, const char** why);
 
 cudaError_t launch_merge_shard_stats(const dllm_shard_stats* shards, int n, int64_t rows,
                                      const dllm_stats& out, cudaStream_t stream);

@@ -160,6 +160,8 @@ struct GemmParams {
   const int32_t* M;
   const int32_t* row_map;  // out row of P row j (-1: skipped); null: j itself
   int32_t* status;
+  int wait_late;           // P and M come from earlier kernels than the one just before this
+                           // one, which only writes the row map: wait for it in the epilogue
 };
 
 // One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
@@ -188,7 +190,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int n_tile = tile % p.n_tiles;
   const int m_pair = tile / p.n_tiles;
   const int m0 = m_pair * 2 * kBM;
-  pdl_wait();  // P, M and the row map come from the kernels before this one
+  // P, M and the row map come from the kernels before this one.  Every kernel of the step
+  // waits for its predecessor before it lets its dependents launch, so when this grid starts,
+  // the kernel two launches back has completed: with wait_late, P and M (written further back)
+  // are complete and only the row map (written by the kernel just before) is waited for, by
+  // the epilogue, while the mainloop overlaps that kernel.
+  if (!p.wait_late) pdl_wait();
   pdl_trigger();
   const int Mdev = *reinterpret_cast<const volatile int32_t*>(p.M);
   if (m0 >= Mdev) return;  // both CTAs of the pair leave together: no row of the pair is kept
@@ -286,6 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
   if (warp >= 4) {
     // ---- epilogue (both CTAs): this CTA's 128 accumulator rows, TMEM -> registers -> global
+    if (p.wait_late) pdl_wait();  // the row map and the output buffers
     __syncwarp();
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int row = my_m0 + q * 32 + lane;
@@ -570,7 +578,7 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
 
 cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const uint16_t* Et,
                                int ldt, float* out, const int32_t* M, const int32_t* row_map,
-                               void* ws, cudaStream_t stream, const char** why) {
+                               bool wait_late, void* ws, cudaStream_t stream, const char** why) {
   const int R_pad = pl.m_tiles * kBM;
   (void)ldt;
   GemmParams gp{};
@@ -601,6 +609,7 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.M = M;
   gp.row_map = row_map;
   gp.status = static_cast<int32_t*>(ws);
+  gp.wait_late = wait_late ? 1 : 0;
   const size_t smem = static_cast<size_t>(pl.stages) * G *
                           (kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2) + 1024;
   cudaError_t e = cudaFuncSetAttribute(smooth_gemm_kernel,
