@@ -680,7 +680,7 @@ def run_loop(args, rank, world, local, key):
                      "traffic": measured_traffic("stats_partials_kernel",
                                                  _FIRST_ITER_CAPTURE.get(key, key)),
                      "ms": ms1, "algorithmic": f"{rows[0]} rows x V x {es} B"},
-        "gpu_launches": 2 * n_it * args.steps,  # statistics + commit per iteration
+        "gpu_launches": (2 * n_it + 1) * args.steps,  # block reset + statistics + commit per iteration
         "clocks": clk,
     }
 

@@ -51,9 +51,6 @@ dllm_status check_shape(const dllm_shape* sh) {
   if (sh->row_stride < sh->V)
     return fail(DLLM_ERR_INVALID_ARG, "row_stride %lld < V %d",
                 static_cast<long long>(sh->row_stride), sh->V);
-  const int es = sh->dtype == DLLM_BF16 ? 2 : 4;
-  if ((sh->row_stride * es) % 16 != 0)
-    return fail(DLLM_ERR_INVALID_ARG, "row_stride*element size must be a multiple of 16 bytes");
   return DLLM_OK;
 }
 
@@ -75,8 +72,21 @@ dllm_status check_state(const dllm_block_state* s) {
   return DLLM_OK;
 }
 
-dllm_status check_logits(const void* logits) {
-  if (!aligned(logits, 16)) return fail(DLLM_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+// Logits for the statistics and commit calls: aligned to their element size (rows that are
+// not 16-byte aligned take the scalar-load path of the statistics kernel).
+dllm_status check_logits(const void* logits, const dllm_shape* sh) {
+  if (!aligned(logits, sh->dtype == DLLM_BF16 ? 2 : 4))
+    return fail(DLLM_ERR_INVALID_ARG, "logits must be aligned to the element size");
+  return DLLM_OK;
+}
+
+// Logits for the smoothing calls: every row 16-byte aligned (vector and asynchronous copies).
+dllm_status check_rows_aligned(const void* logits, const dllm_shape* sh) {
+  const int es = sh->dtype == DLLM_BF16 ? 2 : 4;
+  if (!aligned(logits, 16) || (sh->row_stride * es) % 16 != 0)
+    return fail(DLLM_ERR_UNSUPPORTED,
+                "smoothing needs 16-byte aligned logits rows (pointer and row_stride * element "
+                "size a multiple of 16)");
   return DLLM_OK;
 }
 
@@ -95,7 +105,7 @@ dllm_status commit_common(const void* logits, const dllm_shape* shape, const dll
   DLLM_TRY(check_state(state));
   cudaError_t e;
   if (logits) {
-    DLLM_TRY(check_logits(logits));
+    DLLM_TRY(check_logits(logits, shape));
     DLLM_TRY(check_ws(ws));
     const dllm::StatsWs w = dllm::stats_ws_layout(ws, shape->B, shape->L, shape->V);
     e = dllm::launch_stats_commit(logits, *shape, nullptr, *stats, state, ca, w, sm_count(),
@@ -132,7 +142,7 @@ dllm_status dllm_decode_stats(const void* logits, const dllm_shape* shape, const
                               const dllm_stats* out, void* ws, dllm_stream_t stream) {
   DLLM_TRY(check_shape(shape));
   if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
-  DLLM_TRY(check_logits(logits));
+  DLLM_TRY(check_logits(logits, shape));
   DLLM_TRY(check_stats(out));
   DLLM_TRY(check_ws(ws));
   dllm::CommitArgs ca{};
@@ -292,7 +302,7 @@ dllm_status dllm_smooth_probs(const void* logits, const dllm_shape* shape, const
   dllm::SmoothPlan pl;
   DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
   if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
-  DLLM_TRY(check_logits(logits));
+  DLLM_TRY(check_rows_aligned(logits, shape));
   DLLM_TRY(check_stats(stats));
   DLLM_TRY(check_state(state));
   if (!row_ids || !M) return fail(DLLM_ERR_INVALID_ARG, "row_ids and M must not be null");
@@ -343,7 +353,7 @@ dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* s
   dllm::SmoothPlan pl;
   DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
   if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
-  DLLM_TRY(check_logits(logits));
+  DLLM_TRY(check_rows_aligned(logits, shape));
   DLLM_TRY(check_stats(stats));
   DLLM_TRY(check_state(state));
   if (!Et || !out || !row_ids || !M)

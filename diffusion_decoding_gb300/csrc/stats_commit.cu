@@ -203,6 +203,28 @@ __device__ __forceinline__ RowAcc warp_reduce_slice(const char* row, int64_t e0,
   return RowAcc{m, sum, idx == INT_MAX ? -1 : static_cast<int>(e0) + idx};
 }
 
+// The same reduction for rows that are not 16-byte aligned (a row stride or a logits pointer
+// that is only element-aligned): lane k reads elements k, k + 32, ... one at a time, keeping a
+// running maximum, its first index and the sum of exp(z - maximum), rescaled whenever the
+// maximum rises; the lanes are then merged by shuffles (lowest index on ties).
+template <int DT>
+__device__ __forceinline__ RowAcc warp_reduce_slice_scalar(const char* row, int64_t e0, int n) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY, s = 0.f;
+  int idx = -1;
+  for (int k = lane; k < n; k += 32) {
+    const float x = load_logit(row, DT, e0 + k);
+    if (x > m) {  // s * exp(m - x) + 1; exp(-inf) = 0 for the first element
+      s = fmaf(s, ex2((m - x) * kLog2e), 1.f);
+      m = x;
+      idx = static_cast<int>(e0) + k;
+    } else if (x != -INFINITY) {
+      s += ex2((x - m) * kLog2e);
+    }
+  }
+  return row_acc_warp_reduce(RowAcc{m, s, idx});
+}
+
 // ------------------------------------------------------------------ block helpers
 
 constexpr int kBlockWarpsMax = 32;  // the block helpers below serve blocks of up to 1024 threads
@@ -544,7 +566,7 @@ __device__ __forceinline__ void write_row_stats(const dllm_stats& st, int64_t r,
   st.argmax[r] = a.idx;
 }
 
-template <int DT>
+template <int DT, bool kScalar>
 __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams p) {
   // the block state comes from the kernel before this one (the previous step's commit)
   pdl_wait();
@@ -571,7 +593,9 @@ __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams
   }
   const int64_t e0 = static_cast<int64_t>(sl) * p.chunk;
   const int n = static_cast<int>(min(static_cast<int64_t>(p.V), e0 + p.chunk) - e0);
-  const RowAcc a = warp_reduce_slice<DT>(p.logits + r * p.row_stride_bytes, e0, n);
+  const char* row = p.logits + r * p.row_stride_bytes;
+  const RowAcc a = kScalar ? warp_reduce_slice_scalar<DT>(row, e0, n)
+                           : warp_reduce_slice<DT>(row, e0, n);
   if (lane != 0) return;
   if (S == 1) {  // the slice is the whole row
     write_row_stats(p.stats, r, a);
@@ -790,10 +814,19 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   const int64_t items = static_cast<int64_t>(R) * p.S;
   const dim3 grid1(static_cast<unsigned>((items + kThreads / 32 - 1) / (kThreads / 32)));
   p.pdl_from = std::max(0, static_cast<int>(grid1.x) - 2 * 4 * std::max(1, sm_count));
-  cudaError_t e =
-      sh.dtype == DLLM_BF16
-          ? launch_dependent(stats_partials_kernel<DLLM_BF16>, grid1, dim3(kThreads), 0, stream, p)
-          : launch_dependent(stats_partials_kernel<DLLM_F32>, grid1, dim3(kThreads), 0, stream, p);
+  // rows that are not all 16-byte aligned take the scalar-load reduction
+  const bool scalar = (reinterpret_cast<uintptr_t>(logits) % 16) != 0 || p.row_stride_bytes % 16 != 0;
+  cudaError_t e;
+  if (sh.dtype == DLLM_BF16)
+    e = scalar ? launch_dependent(stats_partials_kernel<DLLM_BF16, true>, grid1, dim3(kThreads), 0,
+                                  stream, p)
+               : launch_dependent(stats_partials_kernel<DLLM_BF16, false>, grid1, dim3(kThreads),
+                                  0, stream, p);
+  else
+    e = scalar ? launch_dependent(stats_partials_kernel<DLLM_F32, true>, grid1, dim3(kThreads), 0,
+                                  stream, p)
+               : launch_dependent(stats_partials_kernel<DLLM_F32, false>, grid1, dim3(kThreads),
+                                  0, stream, p);
   if (e != cudaSuccess) return e;
   if (ca.mode == kStatsOnly && p.S == 1) return cudaSuccess;
   // the merge (+ commit) kernel, one CTA per sequence, as a programmatic dependent launch

@@ -46,7 +46,6 @@ def _shape(**kw):
     (dict(L=1025), dd.DLLM_ERR_UNSUPPORTED),
     (dict(dtype=7), dd.DLLM_ERR_UNSUPPORTED),
     (dict(row_stride=1000), dd.DLLM_ERR_INVALID_ARG),
-    (dict(row_stride=1028), dd.DLLM_ERR_INVALID_ARG),   # 2056 bytes: not a multiple of 16
     (dict(B=2048, L=1024), dd.DLLM_ERR_UNSUPPORTED),
 ])
 def test_shape_validation(lib, kw, expect):
@@ -63,8 +62,16 @@ def test_pointer_validation(lib):
     bs = dd.dllm_block_state(16, 16, 16, 16, 16)
     assert lib.dllm_decode_stats(None, ctypes.byref(sh), None, ctypes.byref(st), 256, None) \
         == dd.DLLM_ERR_INVALID_ARG
-    assert lib.dllm_decode_stats(8, ctypes.byref(sh), None, ctypes.byref(st), 256, None) \
-        == dd.DLLM_ERR_INVALID_ARG  # misaligned logits
+    assert lib.dllm_decode_stats(9, ctypes.byref(sh), None, ctypes.byref(st), 256, None) \
+        == dd.DLLM_ERR_INVALID_ARG  # logits not aligned to the bf16 element
+    # rows that are not 16-byte aligned are read element by element by the statistics calls,
+    # but the smoothing calls need aligned rows
+    odd = _shape(V=1024, row_stride=1028)
+    assert lib.dllm_commit_threshold_smooth(256, ctypes.byref(odd), ctypes.byref(st),
+                                            ctypes.byref(bs), 0.9, -1, 256, 64, 256, 16, 16,
+                                            256, 1 << 30, None) == dd.DLLM_ERR_UNSUPPORTED
+    assert lib.dllm_smooth_probs(258, ctypes.byref(sh), ctypes.byref(st), ctypes.byref(bs), 64,
+                                 16, 16, 256, 1 << 30, None) == dd.DLLM_ERR_UNSUPPORTED
     assert lib.dllm_decode_stats(256, ctypes.byref(sh), None, ctypes.byref(st), 128, None) \
         == dd.DLLM_ERR_INVALID_ARG  # misaligned workspace
     bad = dd.dllm_block_state(16, 0, 16, 16, 16)

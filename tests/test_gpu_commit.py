@@ -98,6 +98,67 @@ def test_stats_padded_row_stride_and_ties():
     assert close(stats.lse.cpu().numpy(), ref.lse)
 
 
+# ------------------------------------------------------------------ rows not 16-byte aligned
+
+def _unaligned(lg: np.ndarray, stride: int, offset: int) -> torch.Tensor:
+    """Rows of lg at `stride` elements, starting `offset` elements into a device buffer; the gaps
+    hold huge values that must never be read."""
+    B, L, V = lg.shape
+    pad = np.uint16(0x7F7F) if lg.dtype == np.uint16 else np.float32(3e38)
+    buf = np.full(offset + B * L * stride, pad, lg.dtype)
+    buf[offset:].reshape(B * L, stride)[:, :V] = lg.reshape(B * L, V)
+    return to_device(buf)[offset:]
+
+
+@pytest.mark.parametrize("V", [1, 7, 9, 2049, 33001])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_stats_unaligned_rows(V, dtype, offset):
+    # stride = V (odd or not a multiple of 16 bytes), logits possibly one element into a buffer
+    w = synth.WORKLOADS["threshold_loop"].scaled(B=3, L=5, V=V, dtype=dtype, eos_id=-1,
+                                                  plant="fixed" if V > 16 else "none")
+    lg = synth.logits(w, seed=V + offset, it=1)
+    rng = np.random.default_rng(V)
+    masked = (rng.random(w.B * w.L) < 0.7).astype(np.uint8)
+    ref = oracle.stats(lg, masked)
+    stats = dd.StatsBuffers(w.B * w.L)
+    shape = dd.make_shape(w.B, w.L, V, dd.DLLM_BF16 if dtype == "bf16" else dd.DLLM_F32,
+                          row_stride=V)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape))
+    dd.dllm_decode_stats(_unaligned(lg, V, offset), shape, torch.from_numpy(masked).cuda(),
+                         stats, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(stats.argmax.cpu().numpy(), ref.argmax)
+    assert close(stats.row_max.cpu().numpy(), ref.row_max, 0.0)
+    assert close(stats.lse.cpu().numpy(), ref.lse)
+    assert close(stats.conf.cpu().numpy(), ref.conf)
+
+
+@pytest.mark.parametrize("key,V,extra,offset,dtype", [
+    ("threshold_loop", 20001, 0, 0, "bf16"),
+    ("threshold_loop", 5003, 0, 1, "f32"),
+    ("hierarchical_loop", 4097, 1, 0, "bf16"),
+    ("credit_loop", 9001, 3, 1, "bf16"),
+])
+def test_loops_on_unaligned_rows(key, V, extra, offset, dtype):
+    w = synth.WORKLOADS[key].scaled(B=2, L=16, V=V, dtype=dtype, max_iters=6)
+    gpu = GpuDecoder(w)
+    gpu.shape = dd.make_shape(w.B, w.L, V, dd.DLLM_BF16 if dtype == "bf16" else dd.DLLM_F32,
+                              row_stride=V + extra)
+    ost = oracle.BlockState(w.B, w.L, w.K)
+    n_done = 0
+    for it in range(w.max_iters):
+        if not ((ost.masked.sum(1) > 0) & (ost.eos_hit == 0)).any():
+            break
+        lg, _, s = guarded_logits(w, 77, it, ost, True)
+        s_ref, scores = oracle_step(w, ost, lg, s)
+        gpu.step(_unaligned(lg, V + extra, offset))
+        torch.cuda.synchronize()
+        _compare_step(gpu, ost, s_ref, scores, tag=f"{key} unaligned iter {it}")
+        n_done += 1
+    assert n_done >= 2
+
+
 def test_stats_deterministic():
     w = synth.WORKLOADS["credit_loop"].scaled(B=4, L=8)
     lg = to_device(synth.logits(w, seed=3))
