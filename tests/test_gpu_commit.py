@@ -212,7 +212,7 @@ def test_credit_loop_full():
     assert n == w.max_iters
 
 
-@pytest.mark.parametrize("K", [8, 3])
+@pytest.mark.parametrize("K", [8, 3, 16])
 def test_credit_calibrated_small(K):
     w = synth.WORKLOADS["credit_loop"].scaled(B=6, L=24, V=12000, K=K, max_iters=20)
     gpu, ost, n = _run_loop(w, 70 + K, calibrated=True)
@@ -227,6 +227,38 @@ def test_large_block_epilogue():
 
 
 # ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("B,L,V,dtype", [(1024, 1024, 8, "bf16"), (2, 3, 2, "f32")])
+def test_extreme_shapes_statistics_and_commit(B, L, V, dtype):
+    # the most rows a call takes (B*L = 2^20, L = 1024) and the smallest vocabulary: statistics
+    # of every row against the oracle, then a threshold no confidence reaches from below
+    # (tau = -1: every masked position commits its argmax), so no decision rests on rounding
+    w = synth.WORKLOADS["threshold_loop"].scaled(B=B, L=L, V=V, dtype=dtype, eos_id=-1,
+                                                  plant="none")
+    lg = synth.logits(w, seed=B + V, it=0)
+    rng = np.random.default_rng(B + V)
+    masked = (rng.random(B * L) < 0.8).astype(np.uint8)
+    ref = oracle.stats(lg, masked)
+    shape = dd.make_shape(B, L, V, dd.DLLM_BF16 if dtype == "bf16" else dd.DLLM_F32)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape))
+    stats = dd.StatsBuffers(B * L)
+    lgd = to_device(lg)
+    dd.dllm_decode_stats(lgd, shape, torch.from_numpy(masked).cuda(), stats, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(stats.argmax.cpu().numpy(), ref.argmax)
+    assert close(stats.row_max.cpu().numpy(), ref.row_max, 0.0)
+    assert close(stats.lse.cpu().numpy(), ref.lse)
+    assert close(stats.conf.cpu().numpy(), ref.conf)
+    state = dd.BlockState(B, L)
+    state.masked.copy_(torch.from_numpy(masked).cuda())
+    dd.dllm_commit_threshold(lgd, shape, stats, state, -1.0, -1, ws)
+    torch.cuda.synchronize()
+    full = oracle.stats(lg)
+    tokens = state.tokens.cpu().numpy()
+    assert np.array_equal(state.committed_now.cpu().numpy(), masked)
+    assert np.array_equal(tokens[masked == 1], full.argmax[masked == 1])
+    assert (tokens[masked == 0] == -1).all() and not state.masked.cpu().numpy().any()
+    assert np.array_equal(state.n_commit.cpu().numpy(), masked.reshape(B, L).sum(1))
 
 def test_stopped_sequences_are_untouched():
     w = synth.WORKLOADS["threshold_loop"].scaled(B=3, L=8, V=512, eos_id=-1)
