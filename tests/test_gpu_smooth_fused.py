@@ -79,6 +79,14 @@ def test_fused_small_all_rows(B, L, V, d):
     assert _fused_case(w, seed=B * 1000 + V, calibrated=True) > 0
 
 
+@pytest.mark.parametrize("d", [16, 65536])
+def test_fused_embedding_width_limits(d):
+    # the narrowest table (one 16-wide column tile) and the widest the call takes (4096 column
+    # tiles of 16 columns per 256-wide pair tile)
+    w = synth.WORKLOADS["smooth_step"].scaled(B=1, L=16, V=1024, d=d, prefix_len=4)
+    assert _fused_case(w, seed=d, calibrated=True) > 0
+
+
 @pytest.mark.parametrize("V,dtype", [
     (1000, "bf16"),    # one CTA per row, a partial last 64-element slab
     (20008, "bf16"),   # clusters of 2, the second CTA's slice ends inside a slab
