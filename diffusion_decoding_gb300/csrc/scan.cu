@@ -1,7 +1,9 @@
-// Warp-scan kernels (kernel "c"): compaction of the rows kept for iteration smoothing, and the
-// neighbourhood KV-refresh mask with its ascending index list.
+// Warp-scan and block-state kernels (kernel "c"): compaction of the rows kept for iteration
+// smoothing (and, for the single-read step, of the rows read before the commit and the map from
+// them to the kept rows), the neighbourhood KV-refresh mask with its ascending index list, and
+// the reset of the decode state for a new block.
 //
-// Both are tiny (at most B*L flags, or P + L cache positions per sequence) and latency-bound; they
+// All are tiny (at most B*L flags, or P + L cache positions per sequence) and latency-bound; they
 // use warp ballots and shuffle prefix sums, never a global barrier.
 #include <algorithm>
 

@@ -2,13 +2,15 @@
 // undecided after this step's commit feed the next round with their whole distribution,
 //   S[j, :] = sum_v bf16(exp(z_{r_j, v} - lse_{r_j})) * E[v, :].
 //
-// Two launches: prob_rows_kernel writes the bf16 probability rows P (compacted), then
-// smooth_gemm_kernel contracts P with the embedding table on the 5th-generation tensor cores.
+// prob_rows_kernel writes the bf16 probability rows P (compacted; the single-read step writes
+// them from its statistics kernel instead), then smooth_gemm_kernel contracts P with the
+// embedding table on the 5th-generation tensor cores (and splitk_reduce_kernel adds the split-K
+// partial sums, in a fixed order, when the plan splits K).
 // Both operands are stored K-slab-blocked, [ceil(V/64)][rows][64]: the 64-wide K slab of every
 // row is contiguous, so the 128 rows a CTA needs from one slab are one contiguous 16 KB run.
-// TMA (3-D tensor maps over the blocked layout, 128-byte swizzle) brings those runs into a
-// multi-stage shared-memory ring; tcgen05.mma accumulates in TMEM; epilogue warps read the
-// accumulator back with tcgen05.ld.
+// TMA (3-D tensor maps over the blocked layout, 128-byte swizzle; two slabs per box) brings
+// those runs into a multi-stage shared-memory ring; tcgen05.mma accumulates in TMEM; epilogue
+// warps read the accumulator back with tcgen05.ld.
 #include <cuda.h>
 
 #include <algorithm>

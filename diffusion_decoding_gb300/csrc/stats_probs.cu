@@ -5,7 +5,7 @@
 // P[j, v] = bf16(exp(z_{r_j, v} - lse_{r_j})) needs the row's log-sum-exp before the first
 // probability can be written, so a row is held on chip while its statistics complete: a cluster
 // of C CTAs shares one row, each CTA bringing its 64-element-aligned slice into shared memory
-// with one bulk copy.  Each CTA reduces its slice to (max, sum of exp(z - max), lowest index of
+// with 16-byte cp.async copies from every thread.  Each CTA reduces its slice to (max, sum of exp(z - max), lowest index of
 // max); the C partials are exchanged through distributed shared memory and merged in rank order
 // by every CTA (so all of them hold the same lse, bit for bit); rank 0 writes the row's
 // statistics and every CTA writes its slice of P, K-slab-blocked, straight from shared memory.
