@@ -741,7 +741,7 @@ def run_reference(args, rank, world):
     value = w.B / sec
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "block-iters/s",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": key, "B": w.B, "L_block": w.L, "V": w.V,
                                         "d": w.d},
