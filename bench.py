@@ -168,8 +168,8 @@ def rank_seed(base: int, rank: int) -> int:
 _KERNEL_SOURCES = {
     "smooth_gemm_kernel": ["smooth.cu", "mbarrier.cuh"],
     "prob_rows_kernel": ["smooth.cu", "mbarrier.cuh"],
-    "stats_partials_kernel": ["stats_commit.cu"],
-    "stats_probs_kernel": ["stats_probs.cu", "mbarrier.cuh"],
+    "stats_partials_kernel": ["stats_commit.cu", "vec_math.cuh"],
+    "stats_probs_kernel": ["stats_probs.cu", "mbarrier.cuh", "vec_math.cuh"],
 }
 
 

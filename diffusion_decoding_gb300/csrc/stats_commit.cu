@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "vec_math.cuh"
 
 namespace dllm {
 namespace {
@@ -56,12 +57,6 @@ struct CommitOnlyParams {
 
 constexpr int kVecs = 8;  // 16-byte vectors per lane: one warp slice = 4 KB
 
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 template <int DT>
 struct SliceTraits;
 template <>
@@ -79,50 +74,6 @@ struct SliceTraits<DLLM_F32> {
 template <int DT>
 constexpr int slice_elems() {
   return 32 * kVecs * SliceTraits<DT>::VEC;
-}
-
-// packed fp32 pairs (one 64-bit register pair) for the fma.rn.f32x2 / add.rn.f32x2 pipes
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-template <int DT>
-__device__ __forceinline__ float vec_max(const uint4& q) {
-  if constexpr (DT == DLLM_BF16) {
-    const uint32_t m = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
-    return fmaxf(bf16lo(m), bf16hi(m));
-  } else {
-    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
-                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
-  }
-}
-
-template <int DT>
-__device__ __forceinline__ void unpack16(const uint4& q, float* x) {
-  if constexpr (DT == DLLM_BF16) {
-    x[0] = bf16lo(q.x); x[1] = bf16hi(q.x);
-    x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
-    x[4] = bf16lo(q.z); x[5] = bf16hi(q.z);
-    x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
-  } else {
-    x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y);
-    x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
-  }
 }
 
 // One warp reduces elements [e0, e0 + n) of a row (n <= slice_elems) to (max, sum of
@@ -171,7 +122,7 @@ __device__ __forceinline__ RowAcc warp_reduce_slice(const char* row, int64_t e0,
 #pragma unroll
   for (int u = 0; u < kVecs; ++u) {
     float x[T::VEC];
-    unpack16<DT>(q[u], x);
+    unpack_vec<DT>(q[u], x);
 #pragma unroll
     for (int j = 0; j < T::VEC; j += 2) {
       float t0, t1;
@@ -190,7 +141,7 @@ __device__ __forceinline__ RowAcc warp_reduce_slice(const char* row, int64_t e0,
     } else {
       const int vi = bu * 32 + lane;
       float x[T::VEC];
-      unpack16<DT>(ld_stream_v4(base + static_cast<int64_t>(vi) * 16), x);
+      unpack_vec<DT>(ld_stream_v4(base + static_cast<int64_t>(vi) * 16), x);
       for (int j = T::VEC - 1; j >= 0; --j)
         if (x[j] == m) idx = vi * T::VEC + j;
     }
