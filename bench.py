@@ -166,8 +166,8 @@ def rank_seed(base: int, rank: int) -> int:
 # Translation units (with the headers they include) whose source a DRAM-traffic figure in
 # profiles/traffic.md was measured on; a figure counts only while that source is unchanged.
 _KERNEL_SOURCES = {
-    "smooth_gemm_kernel": ["smooth.cu", "mbarrier.cuh"],
-    "prob_rows_kernel": ["smooth.cu", "mbarrier.cuh"],
+    "smooth_gemm_kernel": ["smooth.cu", "mbarrier.cuh", "vec_math.cuh"],
+    "prob_rows_kernel": ["smooth.cu", "mbarrier.cuh", "vec_math.cuh"],
     "stats_partials_kernel": ["stats_commit.cu", "vec_math.cuh"],
     "stats_probs_kernel": ["stats_probs.cu", "mbarrier.cuh", "vec_math.cuh"],
 }

@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "mbarrier.cuh"
+#include "vec_math.cuh"
 
 namespace dllm {
 namespace {
@@ -402,16 +403,10 @@ __global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* log
     if (e < V) {
       float x[8];
       if constexpr (DT == DLLM_BF16) {
-        const uint4 q = ld_stream_v4(row + static_cast<int64_t>(e) * 2);
-        x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
-        x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+        unpack_vec<DT>(ld_stream_v4(row + static_cast<int64_t>(e) * 2), x);
       } else {
-        const uint4 q0 = ld_stream_v4(row + static_cast<int64_t>(e) * 4);
-        const uint4 q1 = ld_stream_v4(row + static_cast<int64_t>(e) * 4 + 16);
-        x[0] = __uint_as_float(q0.x); x[1] = __uint_as_float(q0.y);
-        x[2] = __uint_as_float(q0.z); x[3] = __uint_as_float(q0.w);
-        x[4] = __uint_as_float(q1.x); x[5] = __uint_as_float(q1.y);
-        x[6] = __uint_as_float(q1.z); x[7] = __uint_as_float(q1.w);
+        unpack_vec<DT>(ld_stream_v4(row + static_cast<int64_t>(e) * 4), x);
+        unpack_vec<DT>(ld_stream_v4(row + static_cast<int64_t>(e) * 4 + 16), x + 4);
       }
       uint32_t w[4];
 #pragma unroll
