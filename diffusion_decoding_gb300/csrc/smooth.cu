@@ -201,7 +201,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   if (!p.wait_late) pdl_wait();
   pdl_trigger();
   const int Mdev = *reinterpret_cast<const volatile int32_t*>(p.M);
-  if (m0 >= Mdev) return;  // both CTAs of the pair leave together: no row of the pair is kept
+  if (m0 >= Mdev) {
+    // both CTAs of the pair leave together: no row of the pair is kept.  With wait_late this
+    // CTA still waits for the kernel before it: the next launch on the stream waits only for
+    // this grid, so no CTA may finish before the row map (and the block state it reads) is
+    // final, or a following reset could rewrite that state while the map still reads it.
+    if (p.wait_late) pdl_wait();
+    return;
+  }
 
   const int my_m0 = m0 + static_cast<int>(rank) * kBM;
   const int n0 = n_tile * p.bn_base + min(n_tile, p.bn_rem) * 16;

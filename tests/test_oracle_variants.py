@@ -169,3 +169,48 @@ def test_tracked_credit_reduces_to_base_when_one_candidate_is_tracked():
         assert np.array_equal(st_a.cand_id, st_b.cand_id)
         assert np.allclose(st_a.cand_credit, st_b.cand_credit, rtol=1e-12, atol=0)
         assert np.allclose(sc_a, sc_b, rtol=1e-12, atol=0)
+
+
+# ------------------------------------------------------------------ eviction, hand-worked
+
+def _two_logit_row(V, top, second):
+    """fp32 row whose only finite logits are ln(p) of two tokens (p summing to 1): every other
+    token has probability exactly 0."""
+    row = np.full(V, -np.inf, np.float32)
+    for tok, p in (top, second):
+        row[tok] = np.float32(math.log(p))
+    return row
+
+
+def _pair(field):
+    tok, p = field.split(":")
+    return int(tok), float(p)
+
+
+def test_tracked_credit_eviction_hand_traces():
+    # tests/golden/credit_tracked_eviction_hand.txt: K = 2 slots and three candidates, so every
+    # new top-1 token evicts.  Trace 1 is built so that the slot evicted on the credits after
+    # the gains differs from the one evicted on the credits before them (or before the decay);
+    # trace 2 gives exact credit ties (decay 1, untouched tokens gain exactly 0), which must
+    # evict the lowest slot.  The last line of trace 1 commits to a tracked token that is not
+    # the top-1.
+    import golden_io
+    traces = {}
+    for f in golden_io.rows("credit_tracked_eviction_hand.txt"):
+        traces.setdefault(int(f[0]), []).append(f)
+    assert sorted(traces) == [1, 2]
+    V = 16
+    for tid, lines in traces.items():
+        K, decay, boost = int(lines[0][1]), float(lines[0][2]), float(lines[0][3])
+        rows = []
+        for f in lines:
+            watched = _two_logit_row(V, _pair(f[4]), _pair(f[5]))
+            rows.append(np.stack([watched] + _decoys(len(lines), V)))
+        trace = _credit_run(rows, K=K, decay=decay, boost=boost)
+        for it, (f, (score, token, ids, c)) in enumerate(zip(lines, trace), start=1):
+            want_ids = golden_io.ints(f[6])
+            want_c = golden_io.floats(f[7])
+            assert ids.tolist() == want_ids, (tid, it, ids, want_ids)
+            assert np.allclose(c, want_c, rtol=0, atol=1e-6), (tid, it, c, want_c)
+            assert token == int(f[8]), (tid, it, token)
+            assert abs(score - float(f[9])) < 2e-6, (tid, it, score)
