@@ -433,11 +433,13 @@ def run_smooth_step(args, rank, world, local):
         "iters_per_s": 1e3 / ms,
         "ms_per_step_two_pass": ms_two_pass,
         "logit_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
+        # the GEMM is timed on its own (events around one synchronised call), so its scale is
+        # the burst figure; the sustained ratio is kept beside it
         "roofline": {"bound": "tensor", "kernel": "smooth_gemm_kernel", "achieved": gemm_tf,
-                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": gemm_tf / peaks["bf16_tflops_sustained"],
-                     "peak_source": f"{peak_src} bf16 sustained",
-                     "frac_of_burst": gemm_tf / peaks["bf16_tflops"],
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": gemm_tf / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} bf16 burst (kernel timed alone)",
+                     "frac_of_sustained": gemm_tf / peaks["bf16_tflops_sustained"],
                      "traffic": measured_traffic("smooth_gemm_kernel", "smooth_step"),
                      "traffic_unit": "DRAM bytes per launch", "ms": gemm_ms,
                      "algorithmic": f"2*M*V*d = {flops:.4g} FLOP per launch"},

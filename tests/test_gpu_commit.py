@@ -31,22 +31,69 @@ def _compare_step(gpu: GpuDecoder, ost: oracle.BlockState, os_, scores=None, tag
         assert close(hs["cand_credit"], ost.cand_credit), f"{tag}: credits differ"
 
 
-def _run_loop(w, seed, calibrated=False, max_iters=None):
+def _run_loop(w, seed, calibrated=False, max_iters=None, graph=False):
+    """Eager loop checked against the oracle after every iteration.  With graph=True the same
+    loop is then run once more as one CUDA graph (below) on the same device logits."""
     gpu = GpuDecoder(w)
     ost = oracle.BlockState(w.B, w.L, w.K)
     iters = w.max_iters if max_iters is None else max_iters
     n_done = 0
+    kept, n_commits = [], []
     for it in range(iters):
         running = ((ost.masked.sum(1) > 0) & (ost.eos_hit == 0)).any()
         if not running:
             break
         lg, _, s = guarded_logits(w, seed, it, ost, calibrated)
         s_ref, scores = oracle_step(w, ost, lg, s)
-        gpu.step(to_device(lg))
+        lgd = to_device(lg)
+        gpu.step(lgd)
         torch.cuda.synchronize()
         _compare_step(gpu, ost, s_ref, scores, tag=f"{w.key} iter {it}")
         n_done += 1
+        if graph:
+            kept.append(lgd)
+            n_commits.append(ost.n_commit.copy())
+    if graph:
+        _graph_loop_matches_oracle(w, kept, ost, np.array(n_commits), iters)
     return gpu, ost, n_done
+
+
+def _graph_loop_matches_oracle(w, lgs, ost, n_commits, iters):
+    """The whole decode loop as one CUDA graph (dInfer explainer, system optimisations: CUDA
+    graphs and loop unrolling keep the host out of the iterations): the block reset, then
+    `iters` commit calls, each followed by a device copy that records that iteration's n_commit;
+    replayed once over a scribbled state.  Iterations after the oracle's loop has ended reuse
+    its last logits: every sequence is stopped by then, so they must commit nothing.  The final
+    state and every recorded n_commit must equal the oracle trajectory's."""
+    gpu = GpuDecoder(w)
+    rec = torch.full((iters, w.B), -7, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            gpu.state.reset()
+            for it in range(iters):
+                gpu.step(lgs[min(it, len(lgs) - 1)])
+                rec[it].copy_(gpu.state.n_commit)
+    st = gpu.state
+    st.masked.zero_()
+    st.tokens.fill_(12345)
+    st.eos_hit.fill_(1)
+    st.cand_id.fill_(7)
+    st.cand_credit.fill_(2.5)
+    g.replay()
+    torch.cuda.synchronize()
+    hs = gpu.host_state()
+    for k in ("masked", "tokens", "eos_hit"):
+        assert np.array_equal(hs[k], getattr(ost, k)), f"{w.key} graph: {k} differs"
+    if w.strategy == "credit":
+        assert np.array_equal(hs["cand_id"], ost.cand_id), f"{w.key} graph: candidate ids"
+        assert close(hs["cand_credit"], ost.cand_credit), f"{w.key} graph: credits"
+    got = rec.cpu().numpy()
+    n = len(n_commits)
+    assert np.array_equal(got[:n], n_commits), f"{w.key} graph: n_commit per iteration"
+    assert (got[n:] == 0).all(), f"{w.key} graph: iterations after the end committed"
 
 
 # ------------------------------------------------------------------ statistics
@@ -181,20 +228,20 @@ def test_threshold_single_step_full():
 
 def test_threshold_loop_full():
     w = synth.WORKLOADS["threshold_loop"]
-    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key])
+    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key], graph=True)
     assert n >= 1
 
 
 @pytest.mark.parametrize("seed", [5, 6])
 def test_threshold_loop_calibrated_small(seed):
     w = synth.WORKLOADS["threshold_loop"].scaled(B=4, L=32, V=20000)
-    gpu, ost, n = _run_loop(w, seed, calibrated=True)
+    gpu, ost, n = _run_loop(w, seed, calibrated=True, graph=True)
     assert n >= 2
 
 
 def test_hierarchical_loop_full():
     w = synth.WORKLOADS["hierarchical_loop"]
-    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key])
+    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key], graph=True)
     assert ost.masked.sum() == 0
 
 
@@ -202,20 +249,20 @@ def test_hierarchical_loop_full():
 def test_hierarchical_calibrated_small(L, min_width):
     w = synth.WORKLOADS["hierarchical_loop"].scaled(B=5, L=L, V=8200, min_width=min_width,
                                                      max_iters=L)
-    gpu, ost, n = _run_loop(w, 40 + L, calibrated=True)
+    gpu, ost, n = _run_loop(w, 40 + L, calibrated=True, graph=True)
     assert ost.masked.sum() == 0
 
 
 def test_credit_loop_full():
     w = synth.WORKLOADS["credit_loop"]
-    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key])
+    gpu, ost, n = _run_loop(w, synth.workloads.SEEDS[w.key], graph=True)
     assert n == w.max_iters
 
 
 @pytest.mark.parametrize("K", [8, 3, 16])
 def test_credit_calibrated_small(K):
     w = synth.WORKLOADS["credit_loop"].scaled(B=6, L=24, V=12000, K=K, max_iters=20)
-    gpu, ost, n = _run_loop(w, 70 + K, calibrated=True)
+    gpu, ost, n = _run_loop(w, 70 + K, calibrated=True, graph=True)
     assert n >= 5
 
 

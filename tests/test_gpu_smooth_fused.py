@@ -8,7 +8,7 @@ import oracle
 import synth
 from gpu_runner import GpuDecoder, to_device
 from harness import close, guarded_logits, oracle_step
-from test_gpu_smooth import _table, smooth_close
+from test_gpu_smooth import _table, lane_group_sample, smooth_close
 
 import diffusion_decoding_gb300 as dd
 
@@ -26,6 +26,7 @@ def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None,
         ost.eos_hit[:] = eos0
         gpu.state.eos_hit.copy_(torch.from_numpy(eos0.astype(np.int32)).cuda())
     lg, _, s = guarded_logits(w, seed, 0, ost, calibrated)
+    rows_read = np.flatnonzero(oracle.active_rows(ost.masked, ost.eos_hit))
     s_ref, _ = oracle_step(w, ost, lg, s)
     E, Et = _table(w.V, w.d)
     R = w.B * w.L
@@ -59,8 +60,9 @@ def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None,
     assert np.array_equal(rid[:Mg], ids_ref) and (rid[Mg:] == -1).all()
     o = out.cpu().numpy()
     assert np.isnan(o[Mg:]).all(), "rows >= M must stay untouched"
-    js = np.arange(Mg) if sample_rows is None else np.unique(
-        np.linspace(0, Mg - 1, sample_rows).astype(int))
+    # the single-read call's GEMM rows are the rows read (before the commit), in order
+    js = np.arange(Mg) if sample_rows is None else lane_group_sample(
+        np.searchsorted(rows_read, ids_ref))
     ids = ids_ref[js].astype(np.int32)
     ref = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids, E)
     scale = oracle.smooth_embed(lg.reshape(R, w.V), s_ref.lse, ids, E & np.uint16(0x7FFF))
@@ -92,6 +94,8 @@ def test_fused_embedding_width_limits(d):
     (20008, "bf16"),   # clusters of 2, the second CTA's slice ends inside a slab
     (8200, "f32"),     # clusters of 2 over fp32 rows
     (8, "f32"),        # a row of two vectors (smoothing needs V a multiple of 8)
+    (150000, "bf16"),  # rows longer than 8 x 16384 elements: the shared-memory (wide) form
+    (140000, "f32"),
 ])
 def test_fused_ragged_vocab_padded_stride(V, dtype):
     w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=40, V=V, d=48, prefix_len=4, dtype=dtype)
@@ -108,7 +112,7 @@ def test_fused_partial_mask_and_fp32():
 
 def test_fused_full_size_sampled_rows():
     w = synth.WORKLOADS["smooth_step"]
-    Mg = _fused_case(w, synth.workloads.SEEDS[w.key], calibrated=False, sample_rows=6)
+    Mg = _fused_case(w, synth.workloads.SEEDS[w.key], calibrated=False, sample_rows="lanes")
     assert Mg == w.B * w.L - w.B
 
 
@@ -117,3 +121,29 @@ def test_fused_with_a_stopped_sequence():
     eos0 = np.array([0, 1, 0], np.int32)
     Mg = _fused_case(w, seed=9, calibrated=True, eos0=eos0)
     assert 0 < Mg < 2 * w.L
+
+
+def test_fused_step_on_a_finished_block_then_reset():
+    # nothing is masked: no row is read, M = 0 and every GEMM CTA pair leaves at once.  A block
+    # reset launched right behind the step must not overtake the step's kept-row map, which
+    # still reads the (finished) block state: M stays 0 and every row id -1, call after call.
+    w = synth.WORKLOADS["smooth_step"].scaled(B=4, L=64, V=20000, d=256, prefix_len=8)
+    gpu = GpuDecoder(w)
+    E, Et = _table(w.V, w.d)
+    R = w.B * w.L
+    lg = to_device(synth.logits(w, seed=3, calibrated=True))
+    out = torch.full((R, w.d), float("nan"), dtype=torch.float32, device="cuda")
+    row_ids = torch.zeros(R, dtype=torch.int32, device="cuda")
+    M = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+    ws = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
+    for _ in range(20):
+        gpu.state.masked.zero_()
+        dd.dllm_commit_threshold_smooth(lg, gpu.shape, gpu.stats, gpu.state, w.tau, w.eos_id, Et,
+                                        w.d, out, row_ids, M, ws)
+        gpu.state.reset()
+        torch.cuda.synchronize()
+        assert int(M.item()) == 0
+        assert bool((row_ids == -1).all())
+        assert bool((gpu.state.masked == 1).all())
+    assert bool(torch.isnan(out).all()), "no output row may be written"
+    assert dd.dllm_get_status(ws) == dd.DLLM_OK

@@ -15,14 +15,23 @@ import diffusion_decoding_gb300 as dd
 pytestmark = pytest.mark.gpu
 
 
+def _evictions(before: np.ndarray, after: np.ndarray) -> int:
+    """Slots whose tracked token was replaced by another one in a step (an eviction)."""
+    return int(((before >= 0) & (after != before)).sum())
+
+
 def _loop(w, seed, iters, calibrated):
     gpu = GpuDecoder(w)
     ost = oracle.BlockState(w.B, w.L, w.K)
+    ost.evictions = 0
     for it in range(iters):
         if not ost.masked.any():
             break
         lg, _, s = guarded_logits(w, seed, it, ost, calibrated)
+        ids_before = ost.cand_id.copy() if w.K else None
         oracle_step(w, ost, lg, s)
+        if w.K:
+            ost.evictions += _evictions(ids_before, ost.cand_id)
         gpu.step(to_device(lg))
         torch.cuda.synchronize()
         hs = gpu.host_state()
@@ -47,6 +56,29 @@ def test_credit_tracked_loop(calibrated):
     w = synth.WORKLOADS["credit_loop"].scaled(B=8, L=32, V=20000, strategy="credit_tracked",
                                               max_iters=12)
     _loop(w, seed=41, iters=12, calibrated=calibrated)
+
+
+@pytest.mark.parametrize("K", [2, 3])
+@pytest.mark.parametrize("calibrated", [True, False])
+def test_credit_tracked_loop_with_few_slots_evicts(K, calibrated):
+    # with two or three slots every new top-1 token past the first K evicts a tracked one (the
+    # least credit after the gains, lowest slot on ties): the eviction branch runs on many
+    # positions, and slots, credits and commits must still match the oracle every step
+    # (calibrated: the planted token is the position's stable one only 20% of the time, so new
+    # top-1 tokens keep arriving before the confident positions commit)
+    w = synth.WORKLOADS["credit_loop"].scaled(B=8, L=32, V=20000, strategy="credit_tracked",
+                                              K=K, max_iters=16,
+                                              p_stable=0.2 if calibrated else 0.7)
+    st = _loop(w, seed=43 + K, iters=16, calibrated=calibrated)
+    assert st.evictions >= 50, st.evictions
+
+
+@pytest.mark.parametrize("K", [2, 3])
+def test_credit_loop_with_few_slots_evicts(K):
+    # the base credit rule with few slots: evictions by the least decayed credit
+    w = synth.WORKLOADS["credit_loop"].scaled(B=8, L=32, V=20000, K=K, max_iters=16)
+    st = _loop(w, seed=47 + K, iters=16, calibrated=False)
+    assert st.evictions >= 50, st.evictions
 
 
 def test_credit_tracked_needs_logits():
