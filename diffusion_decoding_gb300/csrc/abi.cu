@@ -290,9 +290,9 @@ dllm_status dllm_smooth_plan_info(const dllm_shape* shape, int32_t d, int32_t* i
   info[0] = pl.m_tiles;
   info[1] = pl.n_tiles;
   info[2] = pl.bn_max;
-  info[3] = pl.split_k;
+  info[3] = pl.partials;
   info[4] = pl.stages;
-  info[5] = 3 + (pl.split_k > 1 ? 1 : 0);  // rows, probabilities, GEMM (+ split-K reduction)
+  info[5] = 3 + (pl.partials > 1 ? 1 : 0);  // rows, probabilities, GEMM (+ partial-sum reduction)
   return ok();
 }
 

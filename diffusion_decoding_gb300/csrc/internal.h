@@ -95,12 +95,17 @@ struct SmoothPlan {
   int m_tiles;    // 128-row tiles
   int n_tiles;    // column tiles
   int bn_max;     // widest column tile (multiple of 16, <= 256)
-  int split_k;    // >1: partial sums reduced by a second kernel
+  int split_k;    // K splits of the main pairs (one tile over one split each)
+  int kb_per_split;  // K blocks (64 wide) of each main split
+  int tail_pairs; // pairs that each take tail_tiles tiles over the last K range [kb_tail0, V/64)
+  int tail_tiles;
+  int kb_tail0;
+  int partials;   // K ranges summed per output element (>1: reduced by a second kernel)
   int stages;     // TMA/MMA pipeline depth
   int slabs_per_stage;  // 64-wide K slabs per ring stage (one TMA box of that depth per operand)
   size_t ws_bytes;
   size_t off_p;       // bf16 P, K-slab-blocked [ldp / 64][R_pad][64]
-  size_t off_part;    // fp32 partials [split_k, R_pad, d]
+  size_t off_part;    // fp32 partials [partials, R_pad, d]
   size_t off_rows;    // single-read path: rows read [R], their count, kept index per row [R],
   size_t off_count;   // and kept index per row read [R]
   size_t off_inv;

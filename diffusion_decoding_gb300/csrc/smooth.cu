@@ -151,15 +151,20 @@ struct GemmParams {
   int bn_base;        // narrow pair-tile width; the first bn_rem tiles are 16 wider
   int bn_rem;
   int bn_max;
-  int split_k;
-  int kb_per_split;
+  int split_k;        // K splits of the main pairs (their partial sums 0 .. split_k - 1)
+  int kb_per_split;   // K blocks of each main split
+  int main_pairs;     // pairs [0, main_pairs): one tile over one K split each
+  int tail_pairs;     // pairs after them: tail_tiles tiles each over the tail K range
+  int tail_tiles;
+  int kb_tail0;       // first K block of the tail range (the tail's partial sum is split_k)
   int stages;
   int gs;             // K slabs per stage
   int tmem_cols;
+  int acc_cols;       // TMEM columns between the two accumulators (0: one accumulator)
   int d;
   int R_pad;
-  float* out;          // [M, d] when split_k == 1
-  float* part;         // [split_k, R_pad, d] otherwise
+  float* out;          // [M, d] when there is a single K range
+  float* part;         // [partials, R_pad, d] otherwise
   const int32_t* M;
   const int32_t* row_map;  // out row of P row j (-1: skipped); null: j itself
   int32_t* status;
@@ -167,20 +172,88 @@ struct GemmParams {
                            // one, which only writes the row map: wait for it in the epilogue
 };
 
-// One CTA pair (a 2-CTA cluster) computes a 256 x BN tile of S over one K range.  Both CTAs
-// stream their own 128 rows of P and their own BN/2 rows of E^T through a `stages`-deep ring
-// whose stages hold `gs` consecutive 64-wide K slabs of each operand (one TMA box each).
-// Every stage has its own producer warp (seven of them): once the stage is free it issues the
-// stage's two TMA boxes in its CTA, and both CTAs' boxes complete on the leader CTA's "full"
-// barrier for that stage (the leader's producer posts the byte count of all four boxes).  The
-// leader's MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) and multicasts each
-// stage's release, and finally the accumulator-ready signal, to both CTAs.  No thread relays
-// progress across the pair: an earlier version in which the peer's stages were forwarded by a
-// cluster-scope release arrive spent ~0.7 us per stage on that hop.
+// Bounded wait with acquire at cluster scope (the barrier is arrived at from both CTAs of the
+// pair, after their tensor-memory reads).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
+                                                 volatile int* abort_flag, int32_t* status) {
+  uint64_t t0 = 0;
+  for (uint32_t spins = 0;; ++spins) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((spins & 1023u) == 1023u) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        set_status(status, DLLM_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// One tile of a CTA pair's work: rows m0.. (256), columns n0.. (bn), K blocks kb0.. (nkb),
+// written to partial sum `part_idx` (or straight to the output).
+struct GemmUnit {
+  int m0, n0, bn, kb0, nkb, part_idx;
+};
+
+__device__ __forceinline__ GemmUnit gemm_unit(const GemmParams& p, int pair, int u) {
+  GemmUnit w;
+  int tile;
+  if (pair < p.main_pairs) {
+    const int ks = pair % p.split_k;
+    tile = pair / p.split_k;
+    w.kb0 = ks * p.kb_per_split;
+    const int end = p.tail_pairs > 0 ? p.kb_tail0 : p.num_kb;
+    w.nkb = max(0, min(end, w.kb0 + p.kb_per_split) - w.kb0);
+    w.part_idx = ks;
+  } else {
+    tile = (pair - p.main_pairs) * p.tail_tiles + u;
+    w.kb0 = p.kb_tail0;
+    w.nkb = p.num_kb - p.kb_tail0;
+    w.part_idx = p.split_k;
+  }
+  const int n_tile = tile % p.n_tiles;
+  w.m0 = (tile / p.n_tiles) * 2 * kBM;
+  w.n0 = n_tile * p.bn_base + min(n_tile, p.bn_rem) * 16;
+  w.bn = p.bn_base + (n_tile < p.bn_rem ? 16 : 0);
+  return w;
+}
+
+// A CTA pair (a 2-CTA cluster) computes 256 x BN tiles of S over K ranges: a main pair one
+// tile over one of split_k equal K ranges; a tail pair (the pairs that would otherwise leave
+// SMs idle) a run of tail_tiles tiles, each over the last, short K range, so that every pair
+// of the grid streams about the same number of K blocks.  Both CTAs stream their own 128 rows
+// of P and their own BN/2 rows of E^T through a `stages`-deep ring whose stages hold `gs`
+// consecutive 64-wide K slabs of each operand (one TMA box each), one continuous sequence of
+// stages over the pair's tiles.  Producer warps issue a stage's two TMA boxes in their CTA
+// once the stage is free, and both CTAs' boxes complete on the leader CTA's "full" barrier for
+// that stage (the leader's producer posts the byte count of all four boxes).  The leader's MMA
+// thread issues tcgen05.mma.cta_group::2 (M = 256, N = BN) into one of two TMEM accumulators
+// (alternating by tile), multicasts each stage's release and each tile's accumulator-ready
+// signal to both CTAs; the four epilogue warps of each CTA drain a finished accumulator while
+// the MMAs of the next tile run into the other, and release it on the leader's barrier.  No
+// thread relays ring progress across the pair: an earlier version in which the peer's stages
+// were forwarded by a cluster-scope release arrive spent ~0.7 us per stage on that hop.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     smooth_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t dyn_raw[];
-  __shared__ uint64_t bars[2 * kMaxStages + 1];
+  __shared__ uint64_t bars[2 * kMaxStages + 5];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -188,11 +261,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
-  const int ks = pair % p.split_k;
-  const int tile = pair / p.split_k;
-  const int n_tile = tile % p.n_tiles;
-  const int m_pair = tile / p.n_tiles;
-  const int m0 = m_pair * 2 * kBM;
+  const int m_pairs = p.R_pad / (2 * kBM);
+  const int n_units = pair < p.main_pairs
+                          ? 1
+                          : min(p.tail_tiles, m_pairs * p.n_tiles -
+                                                  (pair - p.main_pairs) * p.tail_tiles);
   // P, M and the row map come from the kernels before this one.  Every kernel of the step
   // waits for its predecessor before it lets its dependents launch, so when this grid starts,
   // the kernel two launches back has completed: with wait_late, P and M (written further back)
@@ -201,7 +274,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   if (!p.wait_late) pdl_wait();
   pdl_trigger();
   const int Mdev = *reinterpret_cast<const volatile int32_t*>(p.M);
-  if (m0 >= Mdev) {
+  // tiles whose rows are all beyond M are skipped (they come last in a pair's run)
+  int U = 0;
+  while (U < n_units && gemm_unit(p, pair, U).m0 < Mdev) ++U;
+  if (U == 0) {
     // both CTAs of the pair leave together: no row of the pair is kept.  With wait_late this
     // CTA still waits for the kernel before it: the next launch on the stream waits only for
     // this grid, so no CTA may finish before the row map (and the block state it reads) is
@@ -209,17 +285,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (p.wait_late) pdl_wait();
     return;
   }
-
-  const int my_m0 = m0 + static_cast<int>(rank) * kBM;
-  const int n0 = n_tile * p.bn_base + min(n_tile, p.bn_rem) * 16;
-  const int bn = p.bn_base + (n_tile < p.bn_rem ? 16 : 0);
-  const int my_n0 = n0 + static_cast<int>(rank) * (bn / 2);
-  const int kb0 = ks * p.kb_per_split;
-  const int nkb = max(0, min(p.num_kb, kb0 + p.kb_per_split) - kb0);
   const int S = p.stages;
-  const int P = min(S, kProducers);
+  const int P = min(S, p.acc_cols > 0 ? 3 : kProducers);  // producers: warps 1..P
   const int G = p.gs;
-  const int nst = (nkb + G - 1) / G;  // ring stages this pair consumes
+  const int nst1 = (gemm_unit(p, pair, 0).nkb + G - 1) / G;  // ring stages per tile
+  const int nst = U * nst1;
+  const bool direct = p.split_k == 1 && p.tail_pairs == 0;  // no partial sums
   const uint32_t b_half_bytes = static_cast<uint32_t>(p.bn_max / 2) * kBK * 2;
   const uint32_t a_stage = static_cast<uint32_t>(G) * kATileBytes;
   const uint32_t b_stage = static_cast<uint32_t>(G) * b_half_bytes;
@@ -230,7 +301,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const uint32_t sB = sbase + S * a_stage;
   const uint32_t full0 = smem_u32(&bars[0]);
   const uint32_t empty0 = smem_u32(&bars[kMaxStages]);
-  const uint32_t acc_bar = smem_u32(&bars[2 * kMaxStages]);
+  const uint32_t accf0 = smem_u32(&bars[2 * kMaxStages]);      // accumulator a ready: + 8a
+  const uint32_t acce0 = smem_u32(&bars[2 * kMaxStages + 2]);  // accumulator a drained: + 8a
+  const uint32_t done_bar = smem_u32(&bars[2 * kMaxStages + 4]);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -238,7 +311,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                     // full barriers are not used)
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf0 + 8 * a, 1);
+      mbar_init(acce0 + 8 * a, 8);  // the four epilogue warps of both CTAs (leader's is used)
+    }
+    mbar_init(done_bar, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -252,7 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_v = &abort_flag;
-  const int prod = warp - 1;  // producer index of warps 1..7
+  const int prod = warp - 1;  // producer index of warps 1..P
 
   int last_k = -1;  // this producer's last issued stage (drained after an abort)
   if (warp >= 1 && prod < P) {
@@ -265,65 +342,98 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       prefetch_tensormap(&p.tmA);
       prefetch_tensormap(&p.tmB);
     }
-    for (int k = prod; k < nst; k += P) {
+    // this producer's position: stage kk of tile u; the tile's coordinates are worked out
+    // once per tile, never between a stage's release and its refill
+    int u = 0, kk = prod;
+    GemmUnit w = gemm_unit(p, pair, 0);
+    int ya = w.m0 + static_cast<int>(rank) * kBM, yb = w.n0 + static_cast<int>(rank) * (w.bn / 2);
+    for (int k = prod; k < nst; k += P, kk += P) {
+      while (kk >= nst1) {
+        kk -= nst1;
+        w = gemm_unit(p, pair, ++u);
+        ya = w.m0 + static_cast<int>(rank) * kBM;
+        yb = w.n0 + static_cast<int>(rank) * (w.bn / 2);
+      }
+      const int slab = w.kb0 + kk * G;
       const int s = k % S;
       const uint32_t ph = (k / S) & 1;
       if (!__all_sync(kFull, wait_bar(empty0 + 8 * s, ph ^ 1, abort_v, p.status))) break;
       if (lane == 0) {
-        const int slab = kb0 + k * G;
         if (leader) mbar_expect_tx(full0 + 8 * s, stage_tx);
-        tma_load_slab_pair(sA + s * a_stage, &p.tmA, leader_full0 + 8 * s, my_m0, slab);
-        tma_load_slab_pair(sB + s * b_stage, &p.tmB, leader_full0 + 8 * s, my_n0, slab);
+        tma_load_slab_pair(sA + s * a_stage, &p.tmA, leader_full0 + 8 * s, ya, slab);
+        tma_load_slab_pair(sB + s * b_stage, &p.tmB, leader_full0 + 8 * s, yb, slab);
       }
       last_k = k;
       __syncwarp();
     }
   } else if (warp == 0 && lane == 0 && leader) {
-    // ---- MMA issuer (leader)
-    const uint32_t idesc = idesc_bf16(2 * kBM, bn);
-    for (int k = 0; k < nst; ++k) {
-      const int s = k % S;
-      const uint32_t ph = (k / S) & 1;
-      if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) break;
-      tc_fence_after();
-      const int nv = min(G, nkb - k * G);  // slabs of this stage inside the pair's K range
-      for (int g = 0; g < nv; ++g) {
-        const uint32_t a_s = sA + s * a_stage + g * kATileBytes;
-        const uint32_t b_s = sB + s * b_stage + g * b_half_bytes;
-#pragma unroll
-        for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-          umma_bf16_pair(tmem, sw128_desc(a_s + kk * kUmmaK * 2),
-                         sw128_desc(b_s + kk * kUmmaK * 2), idesc,
-                         (k > 0 || g > 0 || kk > 0) ? 1u : 0u);
-        }
+    // ---- MMA issuer (leader): tile u into accumulator u % 2
+    bool ok = true;
+    for (int u = 0; u < U && ok; ++u) {
+      const int a = u & 1;
+      // the epilogue warps of both CTAs have drained this accumulator's previous tile
+      if (u >= 2 && !wait_bar_cluster(acce0 + 8 * a, ((u >> 1) - 1) & 1, abort_v, p.status)) {
+        ok = false;
+        break;
       }
-      umma_commit_pair(empty0 + 8 * s);  // stage s is free in both CTAs once these MMAs read it
+      tc_fence_after();
+      const GemmUnit w = gemm_unit(p, pair, u);
+      const uint32_t idesc = idesc_bf16(2 * kBM, w.bn);
+      const uint32_t d_tmem = tmem + static_cast<uint32_t>(a * p.acc_cols);
+      for (int kk = 0; kk < nst1; ++kk) {
+        const int k = u * nst1 + kk;
+        const int s = k % S;
+        const uint32_t ph = (k / S) & 1;
+        if (!wait_bar(full0 + 8 * s, ph, abort_v, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int nv = min(G, w.nkb - kk * G);  // slabs of this stage inside the tile's K range
+        for (int g = 0; g < nv; ++g) {
+          const uint32_t a_s = sA + s * a_stage + g * kATileBytes;
+          const uint32_t b_s = sB + s * b_stage + g * b_half_bytes;
+#pragma unroll
+          for (int k2 = 0; k2 < kBK / kUmmaK; ++k2) {
+            umma_bf16_pair(d_tmem, sw128_desc(a_s + k2 * kUmmaK * 2),
+                           sw128_desc(b_s + k2 * kUmmaK * 2), idesc,
+                           (kk > 0 || g > 0 || k2 > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit_pair(empty0 + 8 * s);  // stage s is free in both CTAs once these MMAs read it
+      }
+      if (ok) umma_commit_pair(accf0 + 8 * a);  // tile u's accumulator complete in both CTAs
     }
-    umma_commit_pair(acc_bar);  // accumulators complete in both CTAs
+    umma_commit_pair(done_bar);  // every MMA issued so far has completed
   }
   if (warp >= 4) {
-    // ---- epilogue (both CTAs): this CTA's 128 accumulator rows, TMEM -> registers -> global
+    // ---- epilogue (both CTAs): this CTA's 128 rows of each finished tile, TMEM -> registers ->
+    // global, then the accumulator is released to the leader's MMA thread
     if (p.wait_late) pdl_wait();  // the row map and the output buffers
     __syncwarp();
     const int q = warp & 3;  // TMEM lane quarter this warp may read
-    const int row = my_m0 + q * 32 + lane;
-    // warp-uniform: tcgen05.ld below is a .sync.aligned warp instruction
-    const bool ok = __all_sync(kFull, wait_bar(acc_bar, 0, abort_v, p.status));
-    tc_fence_after();
-    if (ok) {
-      float* dst_base = p.split_k == 1
-                            ? p.out
-                            : p.part + static_cast<size_t>(ks) * p.R_pad * p.d;
-      // split-K partials keep P's row order; the final rows are mapped by the reduction
+    for (int u = 0; u < U; ++u) {
+      const int a = u & 1;
+      // warp-uniform: tcgen05.ld below is a .sync.aligned warp instruction
+      const bool ok = __all_sync(kFull, wait_bar(accf0 + 8 * a, (u >> 1) & 1, abort_v, p.status));
+      tc_fence_after();
+      if (!ok) break;
+      const GemmUnit w = gemm_unit(p, pair, u);
+      const int row = w.m0 + static_cast<int>(rank) * kBM + q * 32 + lane;
+      float* dst_base =
+          direct ? p.out : p.part + static_cast<size_t>(w.part_idx) * p.R_pad * p.d;
+      // partial sums keep P's row order; the final rows are mapped by the reduction
       const int orow = row >= Mdev ? -1
-                       : (p.split_k == 1 && p.row_map != nullptr) ? __ldg(p.row_map + row) : row;
-      for (int c = 0; c < bn; c += 16) {
+                       : (direct && p.row_map != nullptr) ? __ldg(p.row_map + row) : row;
+      const uint32_t t_acc =
+          tmem + static_cast<uint32_t>(a * p.acc_cols) + (static_cast<uint32_t>(q * 32) << 16);
+      for (int c = 0; c < w.bn; c += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+        tmem_ld16(t_acc + c, v);
         if (orow >= 0) {
           float4* dst =
-              reinterpret_cast<float4*>(dst_base + static_cast<size_t>(orow) * p.d + n0 + c);
-          if (nkb == 0) {
+              reinterpret_cast<float4*>(dst_base + static_cast<size_t>(orow) * p.d + w.n0 + c);
+          if (w.nkb == 0) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0u;
           }
@@ -333,6 +443,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(acce0 + 8 * a, 0));
     }
   }
   tc_fence_before();
@@ -341,10 +454,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     // drain (bounded): MMAs already issued must finish, and TMA boxes still in flight must
     // land, before shared memory and TMEM go away.  Both CTAs' boxes complete on the leader's
     // barriers, and the peer waits at the cluster barrier below until the leader has drained.
-    if (warp == 0 && lane == 0) drain_bar(acc_bar, 0);
     if (leader && last_k >= 0 && lane == 0) drain_bar(full0 + 8 * (last_k % S), (last_k / S) & 1);
     __syncthreads();
   }
+  // every MMA has completed (in both CTAs: the commit is multicast) before TMEM is freed
+  if (warp == 0 && lane == 0) drain_bar(done_bar, 0);
+  __syncthreads();
   cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may still touch it
   if (warp == 0) {
     tc_fence_after();
@@ -506,29 +621,68 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
   const int units16 = d / 16;
   const int num_kb = (V + kBK - 1) / kBK;
   const int pair_slots = std::max(1, sm_count / 2);
-  // Pick (column tiles, split-K) for one wave of CTA pairs, minimising K-blocks per pair x
-  // (BN + 64): wide tiles carry more MMA work per byte staged, and each extra split costs a
-  // round trip of fp32 partial sums.  Only when one wave cannot hold the grid are more waves
-  // allowed (then each wave is charged in full).
+  // Pick (column tiles, split-K, tail pairs) for one wave of CTA pairs, minimising the K blocks
+  // of the busiest pair x (BN + 64): wide tiles carry more MMA work per byte staged, and each
+  // extra K range costs a round trip of fp32 partial sums.  Pair slots that the main pairs
+  // (every tile over split-K equal ranges) leave free take tail pairs: the main ranges stop
+  // short of V and each tail pair runs a few tiles over the remaining K blocks, so that every
+  // pair streams about as many K blocks and no SM idles.  Only when one wave cannot hold the
+  // grid are more waves allowed (then each wave is charged in full).
   double best = 1e300;
   for (int nt = (units16 + 15) / 16; nt <= units16; ++nt) {
     const int base = units16 / nt, rem = units16 % nt;
     const int bn_max = (base + (rem ? 1 : 0)) * 16;
     if (bn_max > 256) continue;
+    const size_t slab_b = kATileBytes + static_cast<size_t>(bn_max / 2) * kBK * 2;
+    const int G = (kMaxDynSmem - 2048) / (2 * slab_b) >= 3 ? 2 : 1;  // slabs per stage
+    const int tiles = m_pairs * nt;
     for (int sk = 1; sk <= std::min(8, num_kb); ++sk) {
-      const long pairs = static_cast<long>(m_pairs) * nt * sk;
+      const long pairs = static_cast<long>(tiles) * sk;
       const long waves = (pairs + pair_slots - 1) / pair_slots;
-      const double kb = static_cast<double>((num_kb + sk - 1) / sk);
-      const double est = (waves > 1 ? 4.0 * waves : 1.0) * kb * (bn_max + 64.0) +
-                         (sk > 1 ? 0.02 * num_kb * 256.0 * sk : 0.0);
+      const int kbs = (num_kb + sk - 1) / sk;
+      const double split_cost = 0.02 * num_kb * 256.0;
+      double est = (waves > 1 ? 4.0 * waves : 1.0) * kbs * (bn_max + 64.0) +
+                   (sk > 1 ? split_cost * sk : 0.0);
+      int tp = 0, tt = 0, km = kbs;
+      const int free_slots = pair_slots - static_cast<int>(pairs);
+      if (waves == 1 && free_slots > 0 && G == 2) {
+        // tail pairs: tt consecutive column tiles of one row pair each, tt dividing the column
+        // tiles (so the tail pairs running at one time read the same few column tiles of E^T,
+        // each shared by every row pair, and a pair keeps its P rows); main ranges of km
+        // blocks (a whole number of stages)
+        int t_tt = 1;
+        while (t_tt <= nt && (nt % t_tt != 0 || tiles / t_tt > free_slots)) ++t_tt;
+        if (t_tt > nt) t_tt = 0;
+        const int t_tp = t_tt > 0 ? tiles / t_tt : 0;
+        int t_km = t_tt > 0
+                       ? static_cast<int>(static_cast<double>(num_kb) * t_tt / (sk * t_tt + 1))
+                       : 0;
+        t_km -= t_km % G;
+        if (t_tt > 0 && t_km >= 8 * G && sk * t_km < num_kb) {
+          const int tail = num_kb - sk * t_km;
+          const double work = std::max(t_km, t_tt * tail + 2 * (t_tt - 1));
+          const double t_est = work * (bn_max + 64.0) + split_cost * (sk + 1);
+          if (t_est < est) {
+            est = t_est;
+            tp = t_tp;
+            tt = t_tt;
+            km = t_km;
+          }
+        }
+      }
       if (est < best - 1e-9) {
         best = est;
         pl.n_tiles = nt;
         pl.bn_max = bn_max;
         pl.split_k = sk;
+        pl.kb_per_split = km;
+        pl.tail_pairs = tp;
+        pl.tail_tiles = tt;
+        pl.kb_tail0 = tp > 0 ? sk * km : num_kb;
       }
     }
   }
+  pl.partials = pl.split_k + (pl.tail_pairs > 0 ? 1 : 0);
   // Two slabs per stage halve the stage hand-offs per MMA (three stages fit); one slab when
   // two would leave fewer than three stages.
   const size_t slab_bytes = kATileBytes + static_cast<size_t>(pl.bn_max / 2) * kBK * 2;
@@ -543,7 +697,7 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
   off += static_cast<size_t>(R_pad) * pl.ldp * 2;
   off = align_up(off, 1024);
   pl.off_part = off;
-  if (pl.split_k > 1) off += static_cast<size_t>(pl.split_k) * R_pad * d * 4;
+  if (pl.partials > 1) off += static_cast<size_t>(pl.partials) * R_pad * d * 4;
   const size_t rows4 = align_up(4 * static_cast<size_t>(pl.R), 256);
   off = align_up(off, 256);
   pl.off_rows = off;
@@ -600,12 +754,22 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
   gp.bn_rem = units16 % pl.n_tiles;
   gp.bn_max = pl.bn_max;
   gp.split_k = pl.split_k;
-  gp.kb_per_split = (gp.num_kb + pl.split_k - 1) / pl.split_k;
+  gp.kb_per_split = pl.kb_per_split;
+  gp.main_pairs = pl.m_tiles / 2 * pl.n_tiles * pl.split_k;
+  gp.tail_pairs = pl.tail_pairs;
+  gp.tail_tiles = pl.tail_tiles;
+  gp.kb_tail0 = pl.kb_tail0;
   gp.stages = pl.stages;
   gp.gs = G;
-  int cols = 32;
-  while (cols < pl.bn_max) cols *= 2;
-  gp.tmem_cols = cols;
+  if (pl.tail_pairs > 0) {  // two accumulators of up to 256 columns: the whole tensor memory
+    gp.tmem_cols = 512;
+    gp.acc_cols = 256;
+  } else {
+    int cols = 32;
+    while (cols < pl.bn_max) cols *= 2;
+    gp.tmem_cols = cols;
+    gp.acc_cols = 0;
+  }
   gp.d = pl.d;
   gp.R_pad = R_pad;
   gp.out = out;
@@ -620,13 +784,13 @@ cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const ui
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  // m_tiles = 2 x row pairs: one CTA per 128 rows, clusters of 2 along x
-  const dim3 grid(static_cast<unsigned>(pl.m_tiles * pl.n_tiles * pl.split_k));
+  // two CTAs (a cluster) per main or tail pair
+  const dim3 grid(static_cast<unsigned>(2 * (gp.main_pairs + gp.tail_pairs)));
   e = launch_dependent(smooth_gemm_kernel, grid, dim3(kGemmThreads), smem, stream, gp);
-  if (e != cudaSuccess || pl.split_k == 1) return e;
+  if (e != cudaSuccess || pl.partials == 1) return e;
   return launch_dependent(splitk_reduce_kernel,
                           dim3(std::min(1024, std::max(1, pl.R * pl.d / 4 / 256))), dim3(256), 0,
-                          stream, static_cast<const float*>(gp.part), pl.split_k, R_pad, pl.d, M,
+                          stream, static_cast<const float*>(gp.part), pl.partials, R_pad, pl.d, M,
                           row_map, out);
 }
 

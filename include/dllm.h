@@ -231,7 +231,9 @@ size_t dllm_smooth_workspace_bytes(const dllm_shape* shape, int32_t d);
 
 /*
  * How dllm_smooth_gemm will run on the current device (host query, launches nothing):
- * info[0] row tiles, info[1] column tiles, info[2] widest column tile, info[3] split-K factor,
+ * info[0] row tiles, info[1] column tiles, info[2] widest column tile, info[3] K ranges summed
+ * per output element (1: the GEMM writes the output itself; more: split-K partial sums added by
+ * a second kernel),
  * info[4] pipeline stages, info[5] kernels launched by one dllm_smooth_embed call.
  */
 dllm_status dllm_smooth_plan_info(const dllm_shape* shape, int32_t d, int32_t* info);
