@@ -4,10 +4,22 @@
 #include <cstdio>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace {
+
+// One NVTX range per entry point, named after it, spanning the host-side work of the call
+// (validation and kernel launches; the kernels themselves run later on the stream).  Free when
+// no profiler is attached.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 thread_local char g_err[512];
 
@@ -80,14 +92,19 @@ dllm_status check_logits(const void* logits, const dllm_shape* sh) {
   return DLLM_OK;
 }
 
-// Logits for the smoothing calls: every row 16-byte aligned (vector and asynchronous copies).
-dllm_status check_rows_aligned(const void* logits, const dllm_shape* sh) {
+// Rows the single-read smoothing kernels can copy whole (16-byte aligned rows, V a multiple of
+// 8); other layouts take the element-wise path.
+bool rows_vector_aligned(const void* logits, const dllm_shape* sh) {
   const int es = sh->dtype == DLLM_BF16 ? 2 : 4;
-  if (!aligned(logits, 16) || (sh->row_stride * es) % 16 != 0)
-    return fail(DLLM_ERR_UNSUPPORTED,
-                "smoothing needs 16-byte aligned logits rows (pointer and row_stride * element "
-                "size a multiple of 16)");
-  return DLLM_OK;
+  return aligned(logits, 16) && (sh->row_stride * es) % 16 == 0 && sh->V % 8 == 0;
+}
+
+dllm::CommitArgs threshold_args(float tau, int32_t eos_id) {
+  dllm::CommitArgs ca{};
+  ca.mode = dllm::kThreshold;
+  ca.tau = tau;
+  ca.eos_id = eos_id;
+  return ca;
 }
 
 #define DLLM_TRY(x)                 \
@@ -140,6 +157,7 @@ size_t dllm_workspace_bytes(const dllm_shape* shape) {
 
 dllm_status dllm_decode_stats(const void* logits, const dllm_shape* shape, const uint8_t* masked,
                               const dllm_stats* out, void* ws, dllm_stream_t stream) {
+  CallRange range_("dllm_decode_stats");
   DLLM_TRY(check_shape(shape));
   if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
   DLLM_TRY(check_logits(logits, shape));
@@ -157,17 +175,16 @@ dllm_status dllm_decode_stats(const void* logits, const dllm_shape* shape, const
 dllm_status dllm_commit_threshold(const void* logits, const dllm_shape* shape,
                                   const dllm_stats* stats, const dllm_block_state* state,
                                   float tau, int32_t eos_id, void* ws, dllm_stream_t stream) {
-  dllm::CommitArgs ca{};
-  ca.mode = dllm::kThreshold;
-  ca.tau = tau;
-  ca.eos_id = eos_id;
-  return commit_common(logits, shape, stats, state, ca, ws, stream, "dllm_commit_threshold");
+  CallRange range_("dllm_commit_threshold");
+  return commit_common(logits, shape, stats, state, threshold_args(tau, eos_id), ws, stream,
+                       "dllm_commit_threshold");
 }
 
 dllm_status dllm_commit_hierarchical(const void* logits, const dllm_shape* shape,
                                      const dllm_stats* stats, const dllm_block_state* state,
                                      float tau_low, int32_t min_width, int32_t eos_id, void* ws,
                                      dllm_stream_t stream) {
+  CallRange range_("dllm_commit_hierarchical");
   if (min_width < 1) return fail(DLLM_ERR_INVALID_ARG, "min_width must be >= 1");
   dllm::CommitArgs ca{};
   ca.mode = dllm::kHierarchical;
@@ -182,6 +199,7 @@ dllm_status dllm_commit_credit(const void* logits, const dllm_shape* shape,
                                int32_t* cand_id, float* cand_credit, int32_t K, float decay,
                                float boost, float tau, int32_t eos_id, void* ws,
                                dllm_stream_t stream) {
+  CallRange range_("dllm_commit_credit");
   if (!cand_id || !cand_credit)
     return fail(DLLM_ERR_INVALID_ARG, "cand_id and cand_credit must not be null");
   if (K < 1 || K > dllm::kMaxK)
@@ -204,6 +222,7 @@ dllm_status dllm_commit_hierarchical_levels(const void* logits, const dllm_shape
                                             const dllm_block_state* state, float tau_low,
                                             int32_t min_width, int32_t eos_id, void* ws,
                                             dllm_stream_t stream) {
+  CallRange range_("dllm_commit_hierarchical_levels");
   if (min_width < 1) return fail(DLLM_ERR_INVALID_ARG, "min_width must be >= 1");
   dllm::CommitArgs ca{};
   ca.mode = dllm::kHierarchicalLevels;
@@ -219,6 +238,7 @@ dllm_status dllm_commit_credit_tracked(const void* logits, const dllm_shape* sha
                                        int32_t* cand_id, float* cand_credit, int32_t K,
                                        float decay, float boost, float tau, int32_t eos_id,
                                        void* ws, dllm_stream_t stream) {
+  CallRange range_("dllm_commit_credit_tracked");
   if (!logits)
     return fail(DLLM_ERR_INVALID_ARG,
                 "logits is null (the tracked-credit variant reads every tracked token's logit)");
@@ -246,6 +266,7 @@ size_t dllm_embedding_t_elems(int32_t V, int32_t d) {
 
 dllm_status dllm_prepare_embedding(const uint16_t* E, int32_t V, int32_t d, uint16_t* Et,
                                    dllm_stream_t stream) {
+  CallRange range_("dllm_prepare_embedding");
   if (!E || !Et) return fail(DLLM_ERR_INVALID_ARG, "E and Et must not be null");
   if (V < 1 || d < 1) return fail(DLLM_ERR_INVALID_ARG, "V and d must be positive");
   if (d % 16 != 0) return fail(DLLM_ERR_UNSUPPORTED, "d=%d is not a multiple of 16", d);
@@ -270,8 +291,6 @@ dllm_status smooth_check(const dllm_shape* shape, int32_t d, void* ws, size_t ws
   DLLM_TRY(check_ws(ws));
   if (d < 16 || d % 16 != 0 || d > 65536)
     return fail(DLLM_ERR_UNSUPPORTED, "d=%d must be a multiple of 16 in [16, 65536]", d);
-  if (shape->V % 8 != 0)
-    return fail(DLLM_ERR_UNSUPPORTED, "smoothing needs V a multiple of 8 (V=%d)", shape->V);
   *pl = dllm::smooth_plan(shape->B, shape->L, shape->V, d, sm_count());
   if (ws_bytes < pl->ws_bytes)
     return fail(DLLM_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
@@ -282,6 +301,7 @@ dllm_status smooth_check(const dllm_shape* shape, int32_t d, void* ws, size_t ws
 }  // namespace
 
 dllm_status dllm_smooth_plan_info(const dllm_shape* shape, int32_t d, int32_t* info) {
+  CallRange range_("dllm_smooth_plan_info");
   DLLM_TRY(check_shape(shape));
   if (!info) return fail(DLLM_ERR_INVALID_ARG, "info is null");
   if (d < 16 || d % 16 != 0 || d > 65536)
@@ -299,10 +319,11 @@ dllm_status dllm_smooth_plan_info(const dllm_shape* shape, int32_t d, int32_t* i
 dllm_status dllm_smooth_probs(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
                               const dllm_block_state* state, int32_t d, int32_t* row_ids,
                               int32_t* M, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  CallRange range_("dllm_smooth_probs");
   dllm::SmoothPlan pl;
   DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
   if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
-  DLLM_TRY(check_rows_aligned(logits, shape));
+  DLLM_TRY(check_logits(logits, shape));
   DLLM_TRY(check_stats(stats));
   DLLM_TRY(check_state(state));
   if (!row_ids || !M) return fail(DLLM_ERR_INVALID_ARG, "row_ids and M must not be null");
@@ -318,6 +339,7 @@ dllm_status dllm_smooth_probs(const void* logits, const dllm_shape* shape, const
 
 dllm_status dllm_smooth_gemm(const dllm_shape* shape, const uint16_t* Et, int32_t d, float* out,
                              const int32_t* M, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  CallRange range_("dllm_smooth_gemm");
   dllm::SmoothPlan pl;
   DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
   if (!Et || !out || !M) return fail(DLLM_ERR_INVALID_ARG, "Et, out and M must not be null");
@@ -338,6 +360,7 @@ dllm_status dllm_smooth_embed(const void* logits, const dllm_shape* shape, const
                               const dllm_block_state* state, const uint16_t* Et, int32_t d,
                               float* out, int32_t* row_ids, int32_t* M, void* ws,
                               size_t ws_bytes, dllm_stream_t stream) {
+  CallRange range_("dllm_smooth_embed");
   if (!Et || !out) return fail(DLLM_ERR_INVALID_ARG, "Et and out must not be null");
   if (!aligned(Et, 16) || !aligned(out, 16))
     return fail(DLLM_ERR_INVALID_ARG, "Et and out must be 16-byte aligned");
@@ -350,10 +373,11 @@ dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* s
                                         float tau, int32_t eos_id, const uint16_t* Et, int32_t d,
                                         float* out, int32_t* row_ids, int32_t* M, void* ws,
                                         size_t ws_bytes, dllm_stream_t stream) {
+  CallRange range_("dllm_commit_threshold_smooth");
   dllm::SmoothPlan pl;
   DLLM_TRY(smooth_check(shape, d, ws, ws_bytes, &pl));
   if (!logits) return fail(DLLM_ERR_INVALID_ARG, "logits is null");
-  DLLM_TRY(check_rows_aligned(logits, shape));
+  DLLM_TRY(check_logits(logits, shape));
   DLLM_TRY(check_stats(stats));
   DLLM_TRY(check_state(state));
   if (!Et || !out || !row_ids || !M)
@@ -361,10 +385,17 @@ dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* s
   if (!aligned(Et, 16) || !aligned(out, 16))
     return fail(DLLM_ERR_INVALID_ARG, "Et and out must be 16-byte aligned");
   int C = 0, per = 0;
-  if (!dllm::stats_probs_split(shape->V, shape->dtype, &C, &per))
-    return fail(DLLM_ERR_UNSUPPORTED,
-                "V=%d is too long for one row per cluster of 8 CTAs; use dllm_commit_threshold "
-                "and dllm_smooth_embed", shape->V);
+  if (!rows_vector_aligned(logits, shape) ||
+      !dllm::stats_probs_split(shape->V, shape->dtype, &C, &per)) {
+    // rows the single-read kernels cannot copy whole (not 16-byte aligned, V not a multiple of
+    // 8, or longer than 8 x 192 KB): the same results from the separate calls, which read such
+    // rows element by element (the logits are read twice)
+    DLLM_TRY(commit_common(logits, shape, stats, state, threshold_args(tau, eos_id),
+                           static_cast<char*>(ws) + pl.off_stats_ws, stream,
+                           "dllm_commit_threshold_smooth"));
+    return dllm_smooth_embed(logits, shape, stats, state, Et, d, out, row_ids, M, ws, ws_bytes,
+                             stream);
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   uint16_t* P = reinterpret_cast<uint16_t*>(w + pl.off_p);
@@ -401,6 +432,7 @@ dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* s
 dllm_status dllm_block_state_reset(const dllm_block_state* state, int32_t B, int32_t L,
                                    int32_t* cand_id, float* cand_credit, int32_t K,
                                    dllm_stream_t stream) {
+  CallRange range_("dllm_block_state_reset");
   DLLM_TRY(check_state(state));
   if (B < 1 || L < 1) return fail(DLLM_ERR_INVALID_ARG, "need B, L >= 1 (B=%d L=%d)", B, L);
   if (L > dllm::kMaxL) return fail(DLLM_ERR_UNSUPPORTED, "L=%d exceeds %d", L, dllm::kMaxL);
@@ -422,6 +454,7 @@ dllm_status dllm_block_state_reset(const dllm_block_state* state, int32_t B, int
 dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32_t L,
                                  int32_t prefix_len, int32_t window, uint8_t* refresh,
                                  int32_t* idx, int32_t* count, dllm_stream_t stream) {
+  CallRange range_("dllm_kv_refresh_mask");
   if (!state || !state->committed_now)
     return fail(DLLM_ERR_INVALID_ARG, "state.committed_now is null");
   if (!refresh || !idx || !count)
@@ -438,6 +471,7 @@ dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32
 }
 
 dllm_status dllm_selftest_wait_timeout(void* ws, uint32_t limit_us, dllm_stream_t stream) {
+  CallRange range_("dllm_selftest_wait_timeout");
   DLLM_TRY(check_ws(ws));
   if (limit_us < 1 || limit_us > 2000000)
     return fail(DLLM_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
@@ -450,6 +484,7 @@ dllm_status dllm_selftest_wait_timeout(void* ws, uint32_t limit_us, dllm_stream_
 
 dllm_status dllm_merge_shard_stats(const dllm_shard_stats* shards, int32_t n, int64_t rows,
                                    const dllm_stats* out, dllm_stream_t stream) {
+  CallRange range_("dllm_merge_shard_stats");
   if (!shards) return fail(DLLM_ERR_INVALID_ARG, "shards is null");
   if (n < 1 || n > DLLM_MAX_SHARDS)
     return fail(DLLM_ERR_INVALID_ARG, "n=%d must be in [1, %d]", n, DLLM_MAX_SHARDS);
@@ -472,6 +507,7 @@ dllm_status dllm_merge_shard_stats(const dllm_shard_stats* shards, int32_t n, in
 }
 
 dllm_status dllm_get_status(void* ws, dllm_stream_t stream, int32_t* out_host) {
+  CallRange range_("dllm_get_status");
   DLLM_TRY(check_ws(ws));
   if (!out_host) return fail(DLLM_ERR_INVALID_ARG, "out_host is null");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -110,6 +110,7 @@ struct SmoothPlan {
   size_t off_count;   // and kept index per row read [R]
   size_t off_inv;
   size_t off_map;
+  size_t off_stats_ws;  // a statistics workspace, for the element-wise single-read fallback
 };
 
 SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count);

@@ -499,8 +499,10 @@ constexpr int kProbThreads = 256;
 
 // P[j, v] = bf16_rn(exp(z_{r_j, v} - lse_{r_j})) for j < M, 8 elements per thread-step, stored
 // K-slab-blocked: element (j, v) at ((v / 64) * R_pad + j) * 64 + v % 64.  The columns of the
-// last slab beyond V are written as zeros (the GEMM reads whole slabs).
-template <int DT>
+// last slab beyond V are written as zeros (the GEMM reads whole slabs).  kScalar: rows that are
+// not 16-byte aligned (an odd row stride, an element-aligned pointer) or V not a multiple of 8
+// are read element by element.
+template <int DT, bool kScalar>
 __global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* logits,
                                                                  int64_t row_stride_bytes, int V,
                                                                  int S, int chunk,
@@ -524,7 +526,10 @@ __global__ void __launch_bounds__(kProbThreads) prob_rows_kernel(const char* log
     uint4 out = make_uint4(0u, 0u, 0u, 0u);
     if (e < V) {
       float x[8];
-      if constexpr (DT == DLLM_BF16) {
+      if constexpr (kScalar) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = e + k < V ? load_logit(row, DT, e + k) : -INFINITY;
+      } else if constexpr (DT == DLLM_BF16) {
         unpack_vec<DT>(ld_stream_v4(row + static_cast<int64_t>(e) * 2), x);
       } else {
         unpack_vec<DT>(ld_stream_v4(row + static_cast<int64_t>(e) * 4), x);
@@ -708,6 +713,9 @@ SmoothPlan smooth_plan(int B, int L, int V, int d, int sm_count) {
   off += rows4;
   pl.off_map = off;
   off += rows4;
+  off = align_up(off, 256);
+  pl.off_stats_ws = off;
+  off += stats_ws_bytes(B, L, V);
   pl.ws_bytes = align_up(off, 256);
   return pl;
 }
@@ -727,11 +735,13 @@ cudaError_t launch_prob_rows(const void* logits, const dllm_shape& sh, const flo
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(R) * S));
   const int64_t rsb = sh.row_stride * es;
   const char* lg = static_cast<const char*>(logits);
-  if (sh.dtype == DLLM_BF16)
-    return launch_dependent(prob_rows_kernel<DLLM_BF16>, grid, dim3(kProbThreads), 0, stream, lg,
-                            rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
-  return launch_dependent(prob_rows_kernel<DLLM_F32>, grid, dim3(kProbThreads), 0, stream, lg,
-                          rsb, sh.V, S, chunk, lse, row_ids, M, P, R_pad);
+  const bool scalar = reinterpret_cast<uintptr_t>(logits) % 16 != 0 || rsb % 16 != 0 ||
+                      sh.V % 8 != 0;
+  auto kern = sh.dtype == DLLM_BF16
+                  ? (scalar ? prob_rows_kernel<DLLM_BF16, true> : prob_rows_kernel<DLLM_BF16, false>)
+                  : (scalar ? prob_rows_kernel<DLLM_F32, true> : prob_rows_kernel<DLLM_F32, false>);
+  return launch_dependent(kern, grid, dim3(kProbThreads), 0, stream, lg, rsb, sh.V, S, chunk, lse,
+                          row_ids, M, P, R_pad);
 }
 
 cudaError_t launch_smooth_gemm(const SmoothPlan& pl, const uint16_t* P, const uint16_t* Et,

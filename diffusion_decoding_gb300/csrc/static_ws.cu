@@ -16,6 +16,8 @@
 // device current, on the first call made on it.
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -54,13 +56,10 @@ dllm_status static_ws_address(void** out) {
   return DLLM_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-dllm_status dllm_commit_threshold_static(const void* logits, const dllm_shape* shape,
-                                         const dllm_stats* stats, const dllm_block_state* state,
-                                         float tau, int32_t eos_id, dllm_stream_t stream) {
+// The call itself (wrapped below in an NVTX range named after the entry point).
+dllm_status commit_static(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
+                          const dllm_block_state* state, float tau, int32_t eos_id,
+                          dllm_stream_t stream) {
   const size_t need = dllm_workspace_bytes(shape);  // 0 when the shape is invalid
   if (need == 0) return fail(DLLM_ERR_INVALID_ARG, "invalid shape");
   if (need > kStaticWsBytes)
@@ -78,6 +77,19 @@ dllm_status dllm_commit_threshold_static(const void* logits, const dllm_shape* s
   cudaError_t e = cudaMemsetAsync(ws, 0, dllm::kWsHeader, s);
   if (e != cudaSuccess) return fail(DLLM_ERR_CUDA, "clearing the static workspace", e);
   return dllm_commit_threshold(logits, shape, stats, state, tau, eos_id, ws, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+dllm_status dllm_commit_threshold_static(const void* logits, const dllm_shape* shape,
+                                         const dllm_stats* stats, const dllm_block_state* state,
+                                         float tau, int32_t eos_id, dllm_stream_t stream) {
+  nvtxRangePushA("dllm_commit_threshold_static");
+  const dllm_status st = commit_static(logits, shape, stats, state, tau, eos_id, stream);
+  nvtxRangePop();
+  return st;
 }
 
 }  // extern "C"

@@ -41,8 +41,8 @@
  *  - logits: B*L rows of V elements, row r starting at element r*row_stride; row_stride >= V.
  *    fp32 or bf16 (dllm_shape.dtype).  The pointer is aligned to the element size.  Rows that
  *    all start on 16-byte boundaries (pointer and row_stride * element size multiples of 16)
- *    are read with 16-byte vector loads; any other layout is read element by element by the
- *    same kernels (slower, same results).  The smoothing calls need the aligned layout.
+ *    are read with 16-byte vector loads; any other layout (and, for the smoothing calls, V not
+ *    a multiple of 8) is read element by element by the same kernels (slower, same results).
  *  - block state (dllm_block_state), all [B, L] or [B] row-major:
  *      masked[B*L]        uint8, 1 = position still undecided;
  *      tokens[B*L]        int32, committed token id, -1 while masked;
@@ -250,8 +250,8 @@ dllm_status dllm_smooth_plan_info(const dllm_shape* shape, int32_t d, int32_t* i
  * Et: the table from dllm_prepare_embedding; d % 16 == 0, d <= 65536;
  * out: [B*L, d] fp32, rows >= M untouched; row_ids: [B*L] int32, entries >= M set to -1;
  * M: one int32.  M is produced on the device; nothing is read back to the host.
- * ws: dllm_smooth_workspace_bytes(shape, d) bytes.  V must be a multiple of 8 and the logits
- * rows 16-byte aligned (pointer and row_stride * element size), else DLLM_ERR_UNSUPPORTED.
+ * ws: dllm_smooth_workspace_bytes(shape, d) bytes.  Logits rows that are not 16-byte aligned,
+ * or V not a multiple of 8, are read element by element (same results).
  */
 dllm_status dllm_smooth_embed(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
                               const dllm_block_state* state, const uint16_t* Et, int32_t d,
@@ -302,8 +302,10 @@ dllm_status dllm_merge_shard_stats(const dllm_shard_stats* shards, int32_t n, in
  * second read; the GEMM then covers the rows read (rows committed in this step included) and
  * writes only the kept ones.
  * ws: dllm_smooth_workspace_bytes(shape, d) bytes; Et prepared by dllm_prepare_embedding.
- * V must be a multiple of 8 and the logits rows 16-byte aligned; DLLM_ERR_UNSUPPORTED for V
- * beyond 8 x 192 KB of one row.
+ * Rows the single-read kernels cannot hold whole (not 16-byte aligned, V not a multiple of 8, or
+ * longer than 8 x 192 KB) give the same results through the separate calls (dllm_commit_threshold
+ * then dllm_smooth_embed, which read rows that are not aligned element by element); the logits
+ * are then read twice.
  */
 dllm_status dllm_commit_threshold_smooth(const void* logits, const dllm_shape* shape,
                                         const dllm_stats* stats, const dllm_block_state* state,

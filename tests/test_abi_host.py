@@ -64,14 +64,14 @@ def test_pointer_validation(lib):
         == dd.DLLM_ERR_INVALID_ARG
     assert lib.dllm_decode_stats(9, ctypes.byref(sh), None, ctypes.byref(st), 256, None) \
         == dd.DLLM_ERR_INVALID_ARG  # logits not aligned to the bf16 element
-    # rows that are not 16-byte aligned are read element by element by the statistics calls,
-    # but the smoothing calls need aligned rows
+    # rows that are not 16-byte aligned are read element by element by every call, but a
+    # pointer not aligned to its element is rejected before anything is launched
     odd = _shape(V=1024, row_stride=1028)
-    assert lib.dllm_commit_threshold_smooth(256, ctypes.byref(odd), ctypes.byref(st),
+    assert lib.dllm_commit_threshold_smooth(257, ctypes.byref(odd), ctypes.byref(st),
                                             ctypes.byref(bs), 0.9, -1, 256, 64, 256, 16, 16,
-                                            256, 1 << 30, None) == dd.DLLM_ERR_UNSUPPORTED
-    assert lib.dllm_smooth_probs(258, ctypes.byref(sh), ctypes.byref(st), ctypes.byref(bs), 64,
-                                 16, 16, 256, 1 << 30, None) == dd.DLLM_ERR_UNSUPPORTED
+                                            256, 1 << 30, None) == dd.DLLM_ERR_INVALID_ARG
+    assert lib.dllm_smooth_probs(259, ctypes.byref(sh), ctypes.byref(st), ctypes.byref(bs), 64,
+                                 16, 16, 256, 1 << 30, None) == dd.DLLM_ERR_INVALID_ARG
     assert lib.dllm_decode_stats(256, ctypes.byref(sh), None, ctypes.byref(st), 128, None) \
         == dd.DLLM_ERR_INVALID_ARG  # misaligned workspace
     bad = dd.dllm_block_state(16, 0, 16, 16, 16)
@@ -100,8 +100,8 @@ def test_pointer_validation(lib):
         == dd.DLLM_ERR_UNSUPPORTED
     assert lib.dllm_prepare_embedding(16, 100, 24, 16, None) == dd.DLLM_ERR_UNSUPPORTED
     assert lib.dllm_smooth_embed(256, ctypes.byref(_shape(V=1020, row_stride=1024)),
-                                 ctypes.byref(st), ctypes.byref(bs), 256, 64, 256, 16, 16, 256,
-                                 1 << 30, None) == dd.DLLM_ERR_UNSUPPORTED
+                                 ctypes.byref(st), ctypes.byref(bs), 256, 40, 256, 16, 16, 256,
+                                 1 << 30, None) == dd.DLLM_ERR_UNSUPPORTED  # d % 16 != 0
     assert lib.dllm_smooth_embed(256, ctypes.byref(sh), ctypes.byref(st), ctypes.byref(bs), 256,
                                  64, 256, 16, 16, 256, 16, None) == dd.DLLM_ERR_INVALID_ARG
     assert lib.dllm_get_status(256, None, None) == dd.DLLM_ERR_INVALID_ARG

@@ -110,6 +110,45 @@ def test_smooth_step_full_sampled_rows():
     assert Mg == w.B * w.L - w.B  # literal workload: one fallback commit per sequence
 
 
+@pytest.mark.parametrize("V,dtype,extra,offset", [
+    (1001, "bf16", 0, 0),     # V not a multiple of 8
+    (20000, "bf16", 3, 1),    # an odd row stride, rows one element off alignment
+    (8191, "f32", 1, 1),
+])
+def test_smooth_unaligned_rows(V, dtype, extra, offset):
+    # the separate calls (commit, then probabilities + GEMM) on rows that are not 16-byte
+    # aligned: the probability rows are read element by element; same results as the oracle
+    from test_gpu_smooth_fused import _layout
+    w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=24, V=V, d=64, prefix_len=4, dtype=dtype)
+    ost = oracle.BlockState(w.B, w.L)
+    lg, _, s = guarded_logits(w, V, 0, ost, True)
+    s_ref, _ = oracle_step(w, ost, lg, s)
+    E, Et = _table(w.V, w.d)
+    R = w.B * w.L
+    dt = dd.DLLM_BF16 if dtype == "bf16" else dd.DLLM_F32
+    shape = dd.make_shape(w.B, w.L, V, dt, row_stride=V + extra)
+    lgd = _layout(lg, V + extra, offset)
+    state, stats = dd.BlockState(w.B, w.L), dd.StatsBuffers(R)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape))
+    ws_s = dd.workspace(dd.dllm_smooth_workspace_bytes(shape, w.d))
+    out = torch.full((R, w.d), float("nan"), dtype=torch.float32, device="cuda")
+    row_ids = torch.empty(R, dtype=torch.int32, device="cuda")
+    M = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dd.dllm_commit_threshold(lgd, shape, stats, state, w.tau, w.eos_id, ws)
+    dd.dllm_smooth_embed(lgd, shape, stats, state, Et, w.d, out, row_ids, M, ws_s)
+    torch.cuda.synchronize()
+    assert np.array_equal(state.masked.cpu().numpy().reshape(w.B, w.L), ost.masked)
+    ids_ref = oracle.smooth_rows(ost.masked, ost.eos_hit)
+    Mg = int(M.item())
+    assert Mg == len(ids_ref) and np.array_equal(row_ids.cpu().numpy()[:Mg], ids_ref)
+    o = out.cpu().numpy()
+    assert np.isnan(o[Mg:]).all()
+    ids = ids_ref.astype(np.int32)
+    ref = oracle.smooth_embed(lg.reshape(R, V), s_ref.lse, ids, E)
+    scale = oracle.smooth_embed(lg.reshape(R, V), s_ref.lse, ids, E & np.uint16(0x7FFF))
+    smooth_close(o[:Mg], ref, scale)
+
+
 def test_smooth_skips_when_nothing_is_masked():
     w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=8, V=1024, d=32)
     gpu = GpuDecoder(w)

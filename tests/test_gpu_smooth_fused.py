@@ -15,8 +15,18 @@ import diffusion_decoding_gb300 as dd
 pytestmark = pytest.mark.gpu
 
 
+def _layout(lg: np.ndarray, stride: int, offset: int) -> torch.Tensor:
+    """Rows of lg at `stride` elements, starting `offset` elements into a device buffer; the gaps
+    hold huge values that must never be read."""
+    B, L, V = lg.shape
+    pad = np.uint16(0x7F7F) if lg.dtype == np.uint16 else np.float32(3e38)
+    buf = np.full(offset + B * L * stride, pad, lg.dtype)
+    buf[offset:].reshape(B * L, stride)[:, :V] = lg.reshape(B * L, V)
+    return to_device(buf)[offset:]
+
+
 def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None,
-                padded=False):
+                padded=False, stride=None, offset=0):
     gpu = GpuDecoder(w)
     ost = oracle.BlockState(w.B, w.L)
     if masked0 is not None:
@@ -35,13 +45,14 @@ def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None,
     M = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
     dt = dd.DLLM_BF16 if w.dtype == "bf16" else dd.DLLM_F32
-    shape, lgd = gpu.shape, lg
+    shape, lgd = gpu.shape, to_device(lg)
     if padded:  # rows padded by 8 elements holding huge values that must never be read
         stride = w.V + 8
-        lgd = np.full((w.B, w.L, stride), 0x7F7F if w.dtype == "bf16" else 3e38, lg.dtype)
-        lgd[:, :, :w.V] = lg
+    if stride is not None or offset:
+        stride = w.V if stride is None else stride
+        lgd = _layout(lg, stride, offset)
         shape = dd.make_shape(w.B, w.L, w.V, dt, row_stride=stride)
-    dd.dllm_commit_threshold_smooth(to_device(lgd), shape, gpu.stats, gpu.state, w.tau,
+    dd.dllm_commit_threshold_smooth(lgd, shape, gpu.stats, gpu.state, w.tau,
                                     w.eos_id, Et, w.d, out, row_ids, M, ws)
     torch.cuda.synchronize()
     assert dd.dllm_get_status(ws) == dd.DLLM_OK
@@ -100,6 +111,20 @@ def test_fused_embedding_width_limits(d):
 def test_fused_ragged_vocab_padded_stride(V, dtype):
     w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=40, V=V, d=48, prefix_len=4, dtype=dtype)
     assert _fused_case(w, seed=V, calibrated=V > 16, padded=True) > 0
+
+
+@pytest.mark.parametrize("V,dtype,extra,offset", [
+    (1001, "bf16", 0, 0),     # V not a multiple of 8
+    (20000, "bf16", 3, 0),    # an odd row stride
+    (20000, "bf16", 0, 1),    # rows one element off 16-byte alignment
+    (8191, "f32", 1, 1),      # all three, fp32
+    (126464, "bf16", 1, 0),   # the full vocabulary at an odd stride
+])
+def test_fused_unaligned_rows_take_the_elementwise_path(V, dtype, extra, offset):
+    # rows the single-read kernels cannot copy whole: same results through the element-wise
+    # statistics and probability kernels
+    w = synth.WORKLOADS["smooth_step"].scaled(B=2, L=24, V=V, d=64, prefix_len=4, dtype=dtype)
+    assert _fused_case(w, seed=V + extra, calibrated=True, stride=V + extra, offset=offset) > 0
 
 
 def test_fused_partial_mask_and_fp32():
