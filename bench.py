@@ -211,6 +211,50 @@ def measured_traffic(kernel: str, workload: str):
     return None
 
 
+def host_numa(local: int) -> dict:
+    """NUMA placement of the host memory the e2e copies come from: the nodes the host has, the
+    node of this GPU's PCI function, and the nodes this process may allocate on."""
+    info = {"host_nodes": None, "gpu_node": None, "allowed_mems": None}
+    base = "/sys/devices/system/node"
+    try:
+        info["host_nodes"] = sorted(int(n[4:]) for n in os.listdir(base)
+                                    if n.startswith("node") and n[4:].isdigit())
+    except OSError:
+        pass
+    try:
+        bus = torch.cuda.get_device_properties(local).pci_bus_id
+        dom = torch.cuda.get_device_properties(local).pci_domain_id
+        dev = torch.cuda.get_device_properties(local).pci_device_id
+        path = f"/sys/bus/pci/devices/{dom:04x}:{bus:02x}:{dev:02x}.0/numa_node"
+        with open(path) as f:
+            info["gpu_node"] = int(f.read().strip())
+    except (OSError, AttributeError, ValueError):
+        pass
+    try:
+        with open("/proc/self/status") as f:
+            for line in f:
+                if line.startswith("Mems_allowed_list:"):
+                    info["allowed_mems"] = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return info
+
+
+def plain_h2d_gbs(nbytes: int, dev) -> float:
+    """One plain pinned host -> device copy of nbytes (cudaMemcpyAsync), best of 5."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = float("inf")
+    for _ in range(6):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(h, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(dev)
+        best = min(best, a.elapsed_time(b))
+    return nbytes / (best * 1e-3) / 1e9
+
+
 def algorithmic_bytes_stats(w, rows_read: int) -> int:
     """Logit bytes one stats launch must read (masked rows only) + state/stat writes."""
     es = 2 if w.dtype == "bf16" else 4
@@ -394,6 +438,9 @@ def run_smooth_step(args, rank, world, local):
     f1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
+    link = host_numa(local)
+    link["plain_h2d_gbs"] = plain_h2d_gbs(h2d, dev)
+    link["e2e_h2d_gbs"] = h2d / (ms_e2e * 1e-3) / 1e9
 
     peaks, peak_src = load_peaks()
     gemm_ms = statistics.mean(t_gemm)
@@ -457,7 +504,8 @@ def run_smooth_step(args, rank, world, local):
                            "traffic": measured_traffic("prob_rows_kernel", "smooth_step")},
         "e2e": {"value": world * B * 1e3 / ms_e2e, "unit": "block-iters/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-                "overlap": "double-buffered: step i+1's logits copy in while step i runs"},
+                "overlap": "double-buffered: step i+1's logits copy in while step i runs",
+                "host_link": link},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
