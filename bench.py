@@ -38,6 +38,13 @@ from synth.workloads import SEEDS, WORKLOADS  # noqa: E402
 METRIC = "decode iters/s per block; logit GB/s as fraction of GB300 HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
+# Decode loops stop on the device: a continue test every k iterations gates the rest of the
+# loop.  A test costs ~6-8 us of graph scheduling (a nested conditional section), so k trades
+# how soon a finished block stops against that cost: 2 for the threshold loop (its blocks end
+# within a few iterations), 8 where blocks decode for tens of iterations (1-2 % over a loop
+# without tests, measured).
+LOOP_TEST_EVERY = {"threshold_loop": 2}
+LOOP_TEST_EVERY_DEFAULT = 8
 
 
 # ------------------------------------------------------------------ environment helpers
@@ -656,27 +663,61 @@ def run_loop(args, rank, world, local, key):
         for lg in lgs:
             one(lg)
 
-    # the whole decode loop (state reset + every iteration) is captured once into a CUDA graph
-    # and replayed: no host round trip or launch gap between iterations; stopped sequences
-    # cost nothing on the device
+    def capture(every: int):
+        """The whole decode loop (state reset + every iteration) as one CUDA graph, replayed per
+        step: no host round trip or launch gap between iterations.  With every = k > 0 the loop
+        stops on the device: before iterations k, 2k, ... dllm_loop_continue tests the block and
+        the rest of the loop sits in a conditional section on that test, each section nested in
+        the one before, so a finished block skips all remaining iterations at the next test."""
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        bodies = [torch.cuda.Stream(dev) for _ in range((n_it - 1) // every if every else 0)]
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                state.reset()
+                cur, level = cap, 0
+                for it in range(n_it):
+                    if every and it > 0 and it % every == 0:
+                        h = dd.dllm_capture_condition(0, cur)
+                        dd.dllm_loop_continue(state, h, cur)
+                        dd.dllm_capture_if_begin(h, bodies[level], cur)
+                        cur, level = bodies[level], level + 1
+                    with torch.cuda.stream(cur):
+                        one(lgs[it])
+                for body in reversed(bodies):
+                    dd.dllm_capture_if_end(body)
+        stream.wait_stream(cap)
+        return g
+
     for _ in range(2):
         loop_eager()
     torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(graph, stream=cap):
-            loop_eager()
-    stream.wait_stream(cap)
+    every = LOOP_TEST_EVERY.get(key, LOOP_TEST_EVERY_DEFAULT)
+    graph_all, graph_es = capture(0), capture(every)
 
-    def loop():
-        graph.replay()
+    def time_graph(g, with_clocks):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        clocks = ClockSampler(local) if with_clocks else None
+        if clocks:
+            clocks.start()
+        load_for(g.replay, 1.5, dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop() if clocks else None
+        return max_over_ranks(e0.elapsed_time(e1) / args.steps, world), clk
 
-    for _ in range(args.warmup):
-        loop()
-    torch.cuda.synchronize(dev)
-    # rows actually read per iteration (masked rows of running sequences), for GB/s
+    ms_all, _ = time_graph(graph_all, False)
+    ms_loop, clk = time_graph(graph_es, True)
+    # rows actually read per iteration (masked rows of running sequences), for GB/s; the
+    # iterations the early-stop loop runs are those that start with a sequence still decoding
     rows = []
     state.reset()
     for lg in lgs:
@@ -685,18 +726,10 @@ def run_loop(args, rank, world, local, key):
         rows.append(int((m.sum(1) * (e == 0)).sum().item()))
         one(lg)
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local)
-    clocks.start()
-    load_for(loop, 1.5, dev)
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        loop()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    ms_loop = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    n_live = 1 + sum(1 for r in rows[1:] if r > 0)  # iterations that start with work to do
+    # iterations the early-stop graph runs: up to the first continue test after the end
+    n_exec = min(n_it, -(-n_live // every) * every)
+    n_tests = (n_exec - 1) // every + (1 if n_exec < n_it else 0)
     # first (fully masked) iteration alone, L2 flushed before each launch
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     t1 = []
@@ -717,16 +750,22 @@ def run_loop(args, rank, world, local, key):
     total_bytes = sum(rows) * w.V * es
     return {
         "metric": METRIC,
-        "value": world * w.B * n_it * 1e3 / ms_loop,
+        "value": world * w.B * n_live * 1e3 / ms_loop,
         "unit": "block-iters/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_loop, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded planted-peak logits)",
-        "config": {"workload": f"{key}: {w.title}", "iterations_per_step": n_it,
-                   "launch": "whole loop captured in one CUDA graph, replayed per step",
+        "config": {"workload": f"{key}: {w.title}", "max_iterations": n_it,
+                   "iterations_decoding": n_live, "iterations_run": n_exec,
+                   "launch": "whole loop captured in one CUDA graph, replayed per step; a "
+                             f"device-side continue test every {every} iterations "
+                             "gates the rest of the loop (nested conditional sections: early "
+                             "stop once every sequence is finished)",
                    "l2": "per-iteration logits pre-generated in HBM and rotated; "
                          "single-iteration timing flushes L2 first"},
-        "iters_per_s": n_it * 1e3 / ms_loop,
+        "iters_per_s": n_live * 1e3 / ms_loop,
+        "loops_per_s": 1e3 / ms_loop,
+        "ms_per_step_all_iterations": ms_all,
         "loop_logit_gbs": total_bytes / (ms_loop * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "stats_partials_kernel + commit_only_kernel (one commit call)", "achieved": gbs1,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs1 / peaks["hbm_gbs"],
@@ -734,7 +773,8 @@ def run_loop(args, rank, world, local, key):
                      "traffic": measured_traffic("stats_partials_kernel",
                                                  _FIRST_ITER_CAPTURE.get(key, key)),
                      "ms": ms1, "algorithmic": f"{rows[0]} rows x V x {es} B"},
-        "gpu_launches": (2 * n_it + 1) * args.steps,  # block reset + statistics + commit per iteration
+        # block reset, statistics + commit per iteration run, the continue tests reached
+        "gpu_launches": (1 + 2 * n_exec + n_tests) * args.steps,
         "clocks": clk,
     }
 

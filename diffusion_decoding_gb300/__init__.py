@@ -104,6 +104,11 @@ _SIGS = {
                                               ctypes.POINTER(dllm_stats),
                                               ctypes.POINTER(dllm_block_state), _c_f32, _c_i32,
                                               _c_vp]),
+    "dllm_capture_condition": (_c_i32, [_c_vp, ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint64)]),
+    "dllm_capture_if_begin": (_c_i32, [_c_vp, _c_vp, ctypes.c_uint64]),
+    "dllm_capture_if_end": (_c_i32, [_c_vp]),
+    "dllm_loop_continue": (_c_i32, [ctypes.POINTER(dllm_block_state), _c_i32, _c_i32,
+                                    ctypes.c_uint64, _c_vp]),
 }
 
 _lib = None
@@ -352,6 +357,32 @@ def dllm_commit_threshold_static(logits, shape, stats: StatsBuffers, state: Bloc
                                               ctypes.byref(st), ctypes.byref(bs), tau, eos_id,
                                               _stream(stream)),
            "dllm_commit_threshold_static")
+
+
+def dllm_capture_condition(default_value: int = 0, stream=None) -> int:
+    """A condition handle in the graph `stream` is capturing (see include/dllm.h)."""
+    h = ctypes.c_uint64(0)
+    _check(lib().dllm_capture_condition(_stream(stream), int(default_value), ctypes.byref(h)),
+           "dllm_capture_condition")
+    return int(h.value)
+
+
+def dllm_capture_if_begin(handle: int, body_stream, stream=None) -> None:
+    """Conditional IF node on `handle` in the graph `stream` is capturing; its body is captured
+    on body_stream until dllm_capture_if_end."""
+    _check(lib().dllm_capture_if_begin(_stream(stream), body_stream.cuda_stream, int(handle)),
+           "dllm_capture_if_begin")
+
+
+def dllm_capture_if_end(body_stream) -> None:
+    _check(lib().dllm_capture_if_end(body_stream.cuda_stream), "dllm_capture_if_end")
+
+
+def dllm_loop_continue(state: BlockState, handle: int, stream=None) -> None:
+    """Inside a capture: sets `handle` to whether some sequence of the block still decodes."""
+    bs = state.c()
+    _check(lib().dllm_loop_continue(ctypes.byref(bs), state.B, state.L, int(handle),
+                                    _stream(stream)), "dllm_loop_continue")
 
 
 def dllm_selftest_wait_timeout(ws, limit_us: int, stream=None) -> None:

@@ -113,6 +113,19 @@ dllm::CommitArgs threshold_args(float tau, int32_t eos_id) {
     if (s_ != DLLM_OK) return s_;   \
   } while (0)
 
+// The graph `stream` is capturing (with its current capture dependencies when asked for);
+// DLLM_ERR_INVALID_ARG when the stream is not capturing.
+dllm_status capturing_graph(dllm_stream_t stream, cudaGraph_t* graph, const cudaGraphNode_t** deps,
+                            size_t* n_deps, const char* name) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamGetCaptureInfo(reinterpret_cast<cudaStream_t>(stream), &cs, nullptr,
+                                           graph, deps, nullptr, n_deps);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  if (cs != cudaStreamCaptureStatusActive)
+    return fail(DLLM_ERR_INVALID_ARG, "%s: stream is not capturing a graph", name);
+  return DLLM_OK;
+}
+
 // Shared body of the three commit entry points.
 dllm_status commit_common(const void* logits, const dllm_shape* shape, const dllm_stats* stats,
                           const dllm_block_state* state, const dllm::CommitArgs& ca, void* ws,
@@ -448,6 +461,79 @@ dllm_status dllm_block_state_reset(const dllm_block_state* state, int32_t B, int
                                                  credit ? n * K : 0,
                                                  reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "dllm_block_state_reset");
+  return ok();
+}
+
+dllm_status dllm_capture_condition(dllm_stream_t stream, uint32_t default_value,
+                                   uint64_t* handle_out) {
+  CallRange range_("dllm_capture_condition");
+  if (!handle_out) return fail(DLLM_ERR_INVALID_ARG, "handle_out is null");
+  cudaGraph_t graph = nullptr;
+  DLLM_TRY(capturing_graph(stream, &graph, nullptr, nullptr, "dllm_capture_condition"));
+  cudaGraphConditionalHandle h = 0;
+  cudaError_t e = cudaGraphConditionalHandleCreate(&h, graph, default_value ? 1u : 0u,
+                                                   cudaGraphCondAssignDefault);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_capture_condition");
+  *handle_out = static_cast<uint64_t>(h);
+  return ok();
+}
+
+dllm_status dllm_capture_if_begin(dllm_stream_t stream, dllm_stream_t body_stream,
+                                  uint64_t handle) {
+  CallRange range_("dllm_capture_if_begin");
+  if (stream == body_stream)
+    return fail(DLLM_ERR_INVALID_ARG, "the conditional body needs a stream of its own");
+  cudaGraph_t graph = nullptr;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t n_deps = 0;
+  DLLM_TRY(capturing_graph(stream, &graph, &deps, &n_deps, "dllm_capture_if_begin"));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t bs = reinterpret_cast<cudaStream_t>(body_stream);
+  cudaStreamCaptureStatus bcs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(bs, &bcs);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_capture_if_begin (body stream)");
+  if (bcs != cudaStreamCaptureStatusNone)
+    return fail(DLLM_ERR_INVALID_ARG, "body_stream is already capturing");
+  cudaGraphNodeParams np = {};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = static_cast<cudaGraphConditionalHandle>(handle);
+  np.conditional.type = cudaGraphCondTypeIf;
+  np.conditional.size = 1;
+  cudaGraphNode_t node = nullptr;
+  e = cudaGraphAddNode(&node, graph, deps, nullptr, n_deps, &np);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_capture_if_begin (conditional node)");
+  // later work on `stream` follows the node; the body is captured on body_stream
+  e = cudaStreamUpdateCaptureDependencies(s, &node, nullptr, 1, cudaStreamSetCaptureDependencies);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_capture_if_begin (dependencies)");
+  e = cudaStreamBeginCaptureToGraph(bs, np.conditional.phGraph_out[0], nullptr, nullptr, 0,
+                                    cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_capture_if_begin (body capture)");
+  return ok();
+}
+
+dllm_status dllm_capture_if_end(dllm_stream_t body_stream) {
+  CallRange range_("dllm_capture_if_end");
+  cudaGraph_t body = nullptr;  // owned by the conditional node
+  cudaError_t e = cudaStreamEndCapture(reinterpret_cast<cudaStream_t>(body_stream), &body);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_capture_if_end");
+  return ok();
+}
+
+dllm_status dllm_loop_continue(const dllm_block_state* state, int32_t B, int32_t L,
+                               uint64_t handle, dllm_stream_t stream) {
+  CallRange range_("dllm_loop_continue");
+  if (!state || !state->masked || !state->eos_hit)
+    return fail(DLLM_ERR_INVALID_ARG, "state.masked and state.eos_hit must not be null");
+  if (B < 1 || L < 1) return fail(DLLM_ERR_INVALID_ARG, "need B, L >= 1 (B=%d L=%d)", B, L);
+  if (L > dllm::kMaxL) return fail(DLLM_ERR_UNSUPPORTED, "L=%d exceeds %d", L, dllm::kMaxL);
+  if (static_cast<int64_t>(B) * L > (int64_t{1} << 20))
+    return fail(DLLM_ERR_UNSUPPORTED, "B*L=%lld exceeds 2^20", static_cast<long long>(B) * L);
+  cudaGraph_t graph = nullptr;  // the handle exists only inside its graph
+  DLLM_TRY(capturing_graph(stream, &graph, nullptr, nullptr, "dllm_loop_continue"));
+  cudaError_t e = dllm::launch_loop_continue(*state, B, L,
+                                             static_cast<cudaGraphConditionalHandle>(handle),
+                                             reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_loop_continue");
   return ok();
 }
 

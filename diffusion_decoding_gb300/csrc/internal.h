@@ -86,6 +86,11 @@ cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int p
                               int window, uint8_t* refresh, int32_t* idx, int32_t* count,
                               cudaStream_t stream);
 
+// Sets a CUDA graph conditional handle to 1 while some sequence of the block still decodes
+// (a masked position, no EOS), else 0.
+cudaError_t launch_loop_continue(const dllm_block_state& state, int B, int L,
+                                 cudaGraphConditionalHandle handle, cudaStream_t stream);
+
 // Smoothing: workspace, probability rows and the tcgen05 GEMM.
 struct SmoothPlan {
   int R;          // rows (upper bound of M)

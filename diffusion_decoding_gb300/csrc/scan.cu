@@ -1,7 +1,8 @@
 // Warp-scan and block-state kernels (kernel "c"): compaction of the rows kept for iteration
 // smoothing (and, for the single-read step, of the rows read before the commit and the map from
-// them to the kept rows), the neighbourhood KV-refresh mask with its ascending index list, and
-// the reset of the decode state for a new block.
+// them to the kept rows), the neighbourhood KV-refresh mask with its ascending index list, the
+// reset of the decode state for a new block, and the device-side test that ends a decode loop
+// captured as a CUDA graph.
 //
 // All are tiny (at most B*L flags, or P + L cache positions per sequence) and latency-bound; they
 // use warp ballots and shuffle prefix sums, never a global barrier.
@@ -221,6 +222,38 @@ cudaError_t launch_block_state_reset(const dllm_block_state& state, int64_t n, i
   const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(1024, (end + 255) / 256));
   return launch_dependent(block_state_reset_kernel, dim3(std::max(1u, blocks)), dim3(256), 0,
                           stream, state, n, B, cand_id, cand_credit, nk);
+}
+
+// Whether the block still decodes: some sequence has a masked position and no EOS.  One CTA
+// (the condition is set exactly once, by thread 0); 16 mask bytes per load where aligned.
+__global__ void __launch_bounds__(1024) loop_continue_kernel(const uint8_t* masked,
+                                                             const int32_t* eos_hit, int B, int L,
+                                                             cudaGraphConditionalHandle handle) {
+  pdl_wait();  // the commit before this one writes the state
+  pdl_trigger();
+  int running = 0;
+  const bool vec = (L % 16) == 0 && (reinterpret_cast<uintptr_t>(masked) % 16) == 0;
+  if (vec) {  // 16 positions of one sequence per load
+    const int per = L / 16;
+    const int64_t nv = static_cast<int64_t>(B) * per;
+    const uint4* m4 = reinterpret_cast<const uint4*>(masked);
+    for (int64_t v = threadIdx.x; v < nv && !running; v += blockDim.x) {
+      const uint4 q = m4[v];
+      if ((q.x | q.y | q.z | q.w) != 0u && eos_hit[v / per] == 0) running = 1;
+    }
+  } else {
+    const int64_t n = static_cast<int64_t>(B) * L;
+    for (int64_t i = threadIdx.x; i < n && !running; i += blockDim.x)
+      if (masked[i] && eos_hit[i / L] == 0) running = 1;
+  }
+  running = __syncthreads_or(running);
+  if (threadIdx.x == 0) cudaGraphSetConditional(handle, running ? 1u : 0u);
+}
+
+cudaError_t launch_loop_continue(const dllm_block_state& state, int B, int L,
+                                 cudaGraphConditionalHandle handle, cudaStream_t stream) {
+  return launch_dependent(loop_continue_kernel, dim3(1), dim3(1024), 0, stream, state.masked,
+                          state.eos_hit, B, L, handle);
 }
 
 cudaError_t launch_kv_refresh(const dllm_block_state& state, int B, int L, int prefix_len,

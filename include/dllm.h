@@ -326,6 +326,58 @@ dllm_status dllm_kv_refresh_mask(const dllm_block_state* state, int32_t B, int32
                                  int32_t* idx, int32_t* count, dllm_stream_t stream);
 
 /*
+ * Device-side early stop for decode loops captured as CUDA graphs (dInfer explainer, system
+ * optimisations: the iterations run back to back on the GPU without waiting on the host, and
+ * decoding stops as soon as the end token is produced instead of running the remaining
+ * iterations).  A caller that captures its whole loop as one graph tests the block every k
+ * iterations and captures the rest of the loop inside a conditional section on that test,
+ * each section nested in the one before:
+ *
+ *   on S0 (capturing):  reset; iterations 0 .. k-1;
+ *                       dllm_capture_condition(S0, 0, &h1); dllm_loop_continue(state, B, L, h1, S0);
+ *                       dllm_capture_if_begin(S0, S1, h1);
+ *     on S1:              iterations k .. 2k-1; the same test and a section on S2; ...
+ *   innermost first:    dllm_capture_if_end(S_n); ... dllm_capture_if_end(S1);
+ *
+ * Once every sequence has stopped, the next test skips everything after it.  A conditional
+ * section costs several microseconds of graph scheduling whether it runs or not (on a GB300:
+ * ~8 us when taken, ~5 us when not, against ~1.4 us per plain kernel node), so a test every
+ * few iterations, not every iteration, pays for itself.
+ *
+ * dllm_capture_condition: `stream` is capturing a CUDA graph (cudaStreamBeginCapture, directly
+ * or through a framework).  Creates a condition handle in that graph with `default_value` (0 or
+ * non-zero -> 1), assigned again at every launch of the graph.  *handle_out receives it.
+ *
+ * dllm_capture_if_begin: adds to the graph `stream` is capturing a conditional IF node on
+ * `handle` (created by dllm_capture_condition on the same capture) that depends on everything
+ * captured on `stream` so far, makes the node `stream`'s only capture dependency (later work
+ * captured on `stream` runs after it) and starts capturing body_stream, another stream that is
+ * not capturing, into the node's body: work enqueued on body_stream until dllm_capture_if_end
+ * runs only when the handle is non-zero when the node is reached.  Sections nest: `stream` may
+ * itself be a body stream.
+ *
+ * dllm_capture_if_end: ends the capture of a body begun by dllm_capture_if_begin (the body graph
+ * belongs to the conditional node).
+ *
+ * dllm_loop_continue: captured in the graph that owns `handle` (at any depth of its conditional
+ * sections); when the graph runs, sets the handle to 1 if some sequence b of the block still
+ * decodes (eos_hit[b] = 0 and a masked position), else 0.  One CTA, ordered after the calls
+ * before it on `stream`.  B >= 1, 1 <= L <= 1024, B*L <= 2^20.
+ *
+ * Errors: DLLM_ERR_INVALID_ARG (a null pointer, stream == body_stream, a stream that must be
+ * capturing and is not, a body_stream already capturing); DLLM_ERR_CUDA (the driver refused the
+ * handle or node, or the body capture was invalidated).  A handle that belongs to another graph
+ * is not detected and must not be passed.
+ */
+dllm_status dllm_capture_condition(dllm_stream_t stream, uint32_t default_value,
+                                   uint64_t* handle_out);
+dllm_status dllm_capture_if_begin(dllm_stream_t stream, dllm_stream_t body_stream,
+                                  uint64_t handle);
+dllm_status dllm_capture_if_end(dllm_stream_t body_stream);
+dllm_status dllm_loop_continue(const dllm_block_state* state, int32_t B, int32_t L,
+                               uint64_t handle, dllm_stream_t stream);
+
+/*
  * Self-test of failure detection (no counterpart in the pages): runs the bounded wait the
  * smoothing GEMM uses on a barrier that nothing ever completes.  After limit_us microseconds
  * (1 .. 2,000,000) the wait gives up and records DLLM_ERR_TIMEOUT in the status word of `ws`

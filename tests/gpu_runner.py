@@ -57,3 +57,37 @@ class GpuDecoder:
         st = self.stats
         return dict(row_max=st.row_max.cpu().numpy(), lse=st.lse.cpu().numpy(),
                     conf=st.conf.cpu().numpy(), argmax=st.argmax.cpu().numpy())
+
+
+def capture_loop(gpu: GpuDecoder, lgs, iters: int, every: int = 0, rec=None):
+    """The whole decode loop as one CUDA graph: the block reset, then `iters` commit calls
+    (iteration it on lgs[min(it, len(lgs) - 1)]), each followed by a device copy of that
+    iteration's n_commit into rec[it] when rec is given.  With every = k > 0 the loop stops on
+    the device: before iterations k, 2k, ... dllm_loop_continue tests the block and the rest of
+    the loop is captured inside a conditional section on that test, each section nested in the
+    one before, so once the block is finished the remaining iterations do not run at all (their
+    rec rows keep whatever they held)."""
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    depth = (iters - 1) // every if every else 0
+    bodies = [torch.cuda.Stream() for _ in range(depth)]  # one per nesting level
+    cap.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            gpu.state.reset()
+            cur, level = cap, 0
+            for it in range(iters):
+                if every and it > 0 and it % every == 0:
+                    h = dd.dllm_capture_condition(0, cur)
+                    dd.dllm_loop_continue(gpu.state, h, cur)
+                    dd.dllm_capture_if_begin(h, bodies[level], cur)
+                    cur, level = bodies[level], level + 1
+                with torch.cuda.stream(cur):
+                    gpu.step(lgs[min(it, len(lgs) - 1)])
+                    if rec is not None:
+                        rec[it].copy_(gpu.state.n_commit)
+            for body in reversed(bodies):
+                dd.dllm_capture_if_end(body)
+    torch.cuda.current_stream().wait_stream(cap)
+    return g

@@ -105,6 +105,13 @@ def test_pointer_validation(lib):
     assert lib.dllm_smooth_embed(256, ctypes.byref(sh), ctypes.byref(st), ctypes.byref(bs), 256,
                                  64, 256, 16, 16, 256, 16, None) == dd.DLLM_ERR_INVALID_ARG
     assert lib.dllm_get_status(256, None, None) == dd.DLLM_ERR_INVALID_ARG
+    # loop capture: checked before any CUDA call
+    assert lib.dllm_capture_condition(None, 0, None) == dd.DLLM_ERR_INVALID_ARG
+    assert lib.dllm_capture_if_begin(16, 16, 1) == dd.DLLM_ERR_INVALID_ARG  # one stream for both
+    no_mask = dd.dllm_block_state(None, 16, 16, 16, 16)
+    assert lib.dllm_loop_continue(ctypes.byref(no_mask), 2, 8, 1, None) == dd.DLLM_ERR_INVALID_ARG
+    assert lib.dllm_loop_continue(ctypes.byref(bs), 0, 8, 1, None) == dd.DLLM_ERR_INVALID_ARG
+    assert lib.dllm_loop_continue(ctypes.byref(bs), 2, 1025, 1, None) == dd.DLLM_ERR_UNSUPPORTED
 
 
 def test_workspace_sizes(lib):

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from gpu_runner import GpuDecoder, to_device
+from gpu_runner import GpuDecoder, capture_loop, to_device
 from harness import close, guarded_logits, oracle_step
 
 import diffusion_decoding_gb300 as dd
@@ -60,40 +60,43 @@ def _run_loop(w, seed, calibrated=False, max_iters=None, graph=False):
 
 def _graph_loop_matches_oracle(w, lgs, ost, n_commits, iters):
     """The whole decode loop as one CUDA graph (dInfer explainer, system optimisations: CUDA
-    graphs and loop unrolling keep the host out of the iterations): the block reset, then
-    `iters` commit calls, each followed by a device copy that records that iteration's n_commit;
-    replayed once over a scribbled state.  Iterations after the oracle's loop has ended reuse
-    its last logits: every sequence is stopped by then, so they must commit nothing.  The final
-    state and every recorded n_commit must equal the oracle trajectory's."""
-    gpu = GpuDecoder(w)
-    rec = torch.full((iters, w.B), -7, dtype=torch.int32, device="cuda")
-    s = torch.cuda.Stream()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            gpu.state.reset()
-            for it in range(iters):
-                gpu.step(lgs[min(it, len(lgs) - 1)])
-                rec[it].copy_(gpu.state.n_commit)
-    st = gpu.state
-    st.masked.zero_()
-    st.tokens.fill_(12345)
-    st.eos_hit.fill_(1)
-    st.cand_id.fill_(7)
-    st.cand_credit.fill_(2.5)
-    g.replay()
-    torch.cuda.synchronize()
-    hs = gpu.host_state()
-    for k in ("masked", "tokens", "eos_hit"):
-        assert np.array_equal(hs[k], getattr(ost, k)), f"{w.key} graph: {k} differs"
-    if w.strategy == "credit":
-        assert np.array_equal(hs["cand_id"], ost.cand_id), f"{w.key} graph: candidate ids"
-        assert close(hs["cand_credit"], ost.cand_credit), f"{w.key} graph: credits"
-    got = rec.cpu().numpy()
+    graphs and loop unrolling keep the host out of the iterations), plain and stopping on the
+    device (a continue test every 4 iterations, and every iteration on short loops).  Each form
+    is replayed twice over a scribbled state; iteration it records its n_commit in rec[it].
+    Iterations after the oracle's loop has ended reuse its last logits: every sequence is
+    stopped by then, so an iteration that runs must commit nothing, and with the device stop
+    only the iterations up to the next test after the end may run (the rest keep the fill
+    value).  The final state and every recorded n_commit must equal the oracle trajectory's."""
     n = len(n_commits)
-    assert np.array_equal(got[:n], n_commits), f"{w.key} graph: n_commit per iteration"
-    assert (got[n:] == 0).all(), f"{w.key} graph: iterations after the end committed"
+    forms = [0, 4] + ([1] if iters <= 24 else [])
+    for every in forms:
+        gpu = GpuDecoder(w)
+        rec = torch.empty((iters, w.B), dtype=torch.int32, device="cuda")
+        g = capture_loop(gpu, lgs, iters, every, rec)
+        tag = f"{w.key} graph (test every {every})"
+        # with a test every k iterations, the iterations after the end that still run are
+        # those before the first test that comes after the end
+        ran_to = iters if every == 0 else min(iters, -(-n // every) * every)
+        for rep in range(2):
+            st = gpu.state
+            st.masked.zero_()
+            st.tokens.fill_(12345)
+            st.eos_hit.fill_(1)
+            st.cand_id.fill_(7)
+            st.cand_credit.fill_(2.5)
+            rec.fill_(-7)
+            g.replay()
+            torch.cuda.synchronize()
+            hs = gpu.host_state()
+            for k in ("masked", "tokens", "eos_hit"):
+                assert np.array_equal(hs[k], getattr(ost, k)), f"{tag} {rep}: {k} differs"
+            if w.strategy == "credit":
+                assert np.array_equal(hs["cand_id"], ost.cand_id), f"{tag} {rep}: candidate ids"
+                assert close(hs["cand_credit"], ost.cand_credit), f"{tag} {rep}: credits"
+            got = rec.cpu().numpy()
+            assert np.array_equal(got[:n], n_commits), f"{tag} {rep}: n_commit per iteration"
+            assert (got[n:ran_to] == 0).all(), f"{tag} {rep}: iterations after the end committed"
+            assert (got[ran_to:] == -7).all(), f"{tag} {rep}: iterations after a stop ran"
 
 
 # ------------------------------------------------------------------ statistics
