@@ -26,7 +26,7 @@ def _layout(lg: np.ndarray, stride: int, offset: int) -> torch.Tensor:
 
 
 def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None,
-                padded=False, stride=None, offset=0):
+                padded=False, stride=None, offset=0, ws=None):
     gpu = GpuDecoder(w)
     ost = oracle.BlockState(w.B, w.L)
     if masked0 is not None:
@@ -43,7 +43,8 @@ def _fused_case(w, seed, calibrated, sample_rows=None, masked0=None, eos0=None,
     out = torch.full((R, w.d), float("nan"), dtype=torch.float32, device="cuda")
     row_ids = torch.empty(R, dtype=torch.int32, device="cuda")
     M = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
+    if ws is None:
+        ws = dd.workspace(dd.dllm_smooth_workspace_bytes(gpu.shape, w.d))
     dt = dd.DLLM_BF16 if w.dtype == "bf16" else dd.DLLM_F32
     shape, lgd = gpu.shape, to_device(lg)
     if padded:  # rows padded by 8 elements holding huge values that must never be read
@@ -171,4 +172,20 @@ def test_fused_step_on_a_finished_block_then_reset():
         assert bool((row_ids == -1).all())
         assert bool((gpu.state.masked == 1).all())
     assert bool(torch.isnan(out).all()), "no output row may be written"
+    assert dd.dllm_get_status(ws) == dd.DLLM_OK
+
+
+def test_fused_calls_share_a_workspace_across_shapes():
+    # One smoothing workspace, sized for the largest shape, serves calls of three shapes in turn,
+    # twice (the first shape's plan splits K: partial sums in the workspace, added in a fixed
+    # order); every call matches the oracle.
+    shapes = [dict(B=4, L=64, V=126464, d=512), dict(B=2, L=64, V=20000, d=272),
+              dict(B=3, L=100, V=2056, d=160)]
+    ws_list = [synth.WORKLOADS["smooth_step"].scaled(prefix_len=16, **kw) for kw in shapes]
+    need = max(dd.dllm_smooth_workspace_bytes(GpuDecoder(w).shape, w.d) for w in ws_list)
+    ws = dd.workspace(need)
+    assert dd.dllm_smooth_plan_info(GpuDecoder(ws_list[0]).shape, ws_list[0].d)["split_k"] > 1
+    for rep in range(2):
+        for i, w in enumerate(ws_list):
+            assert _fused_case(w, seed=100 * rep + i, calibrated=True, ws=ws) > 0
     assert dd.dllm_get_status(ws) == dd.DLLM_OK
