@@ -268,6 +268,34 @@ def algorithmic_bytes_stats(w, rows_read: int) -> int:
     return rows_read * w.V * es
 
 
+def capture_graph(fn, dev, stream):
+    """fn() captured once as a CUDA graph (on a side stream, joined back to `stream`)."""
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+    stream.wait_stream(cap)
+    return g
+
+
+def cold_replay_ms(g, flush, dev, stream, n=40):
+    """Mean time of one replay of g between two events, each after an L2 flush (a write of a
+    buffer twice the L2) on a GPU kept busy while the host enqueues the replay."""
+    ts = []
+    for _ in range(n):
+        flush.fill_(1)
+        torch.cuda._sleep(1_000_000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts)
+
+
 def run_smooth_step(args, rank, world, local):
     import diffusion_decoding_gb300 as dd
 
@@ -375,6 +403,18 @@ def run_smooth_step(args, rank, world, local):
         t_stats.append(ev["a0"].elapsed_time(ev["a1"]))
         t_prob.append(ev["a1"].elapsed_time(ev["b0"]))
         t_gemm.append(ev["b0"].elapsed_time(ev["b1"]))
+
+    # the statistics + commit call inside a graph, as a captured step runs it: a graph of the
+    # block reset + the call against one of the reset alone, each replayed after an L2 flush
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    g_reset = capture_graph(reset_state, dev, stream)
+    g_call = capture_graph(
+        lambda: (reset_state(),
+                 dd.dllm_commit_threshold(logits, shape, stats, state, w.tau, w.eos_id, ws)),
+        dev, stream)
+    stats_ms_graph = (cold_replay_ms(g_call, flush, dev, stream) -
+                      cold_replay_ms(g_reset, flush, dev, stream))
+    del flush
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -504,6 +544,9 @@ def run_smooth_step(args, rank, world, local):
                            "traffic": measured_traffic("stats_partials_kernel", "smooth_step"),
                            "traffic_unit": "DRAM bytes per launch (statistics kernel)",
                            "ms": stats_ms,
+                           "ms_in_graph": stats_ms_graph,
+                           "frac_in_graph": stats_bytes / (stats_ms_graph * 1e-3) / 1e9
+                                            / peaks["hbm_gbs"],
                            "algorithmic": f"{stats_bytes} logit bytes per launch"},
         "roofline_probs": {"bound": "hbm", "kernel": "prob_rows_kernel", "achieved": prob_gbs,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -743,6 +786,13 @@ def run_loop(args, rank, world, local, key):
         b.record(stream)
         torch.cuda.synchronize(dev)
         t1.append(a.elapsed_time(b))
+    # the same first iteration inside a graph (as the loops run it): a graph of the block reset
+    # + the first call against a graph of the reset alone, each replayed cold; the difference is
+    # what the first iteration adds to a captured loop
+    g_reset = capture_graph(state.reset, dev, stream)
+    g_first = capture_graph(lambda: (state.reset(), one(lgs[0])), dev, stream)
+    ms1_graph = (cold_replay_ms(g_first, flush, dev, stream) -
+                 cold_replay_ms(g_reset, flush, dev, stream))
     peaks, peak_src = load_peaks()
     es = 2 if w.dtype == "bf16" else 4
     ms1 = statistics.median(t1)
@@ -772,7 +822,10 @@ def run_loop(args, rank, world, local, key):
                      "peak_source": f"{peak_src} HBM copy",
                      "traffic": measured_traffic("stats_partials_kernel",
                                                  _FIRST_ITER_CAPTURE.get(key, key)),
-                     "ms": ms1, "algorithmic": f"{rows[0]} rows x V x {es} B"},
+                     "ms": ms1, "ms_in_graph": ms1_graph,
+                     "frac_in_graph": rows[0] * w.V * es / (ms1_graph * 1e-3) / 1e9
+                                      / peaks["hbm_gbs"],
+                     "algorithmic": f"{rows[0]} rows x V x {es} B"},
         # block reset, statistics + commit per iteration run, the continue tests reached
         "gpu_launches": (1 + 2 * n_exec + n_tests) * args.steps,
         "clocks": clk,
