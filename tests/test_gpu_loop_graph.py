@@ -152,6 +152,35 @@ def test_loop_continue_reads_stopped_sequences(L):
         assert int(ran.item()) == expect, (int(masked.sum()), eos)
 
 
+def test_loop_continue_on_the_largest_block():
+    # B*L = 2^20 positions (1024 x 1024): one CTA tests 65,536 16-byte vectors of mask bytes
+    B = L = 1024
+    state = dd.BlockState(B, L)
+    s2 = torch.cuda.Stream()
+    ran = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def body(cap):
+        h = dd.dllm_capture_condition(0, cap)
+        dd.dllm_loop_continue(state, h, cap)
+        dd.dllm_capture_if_begin(h, s2, cap)
+        with torch.cuda.stream(s2):
+            ran.add_(1)
+        dd.dllm_capture_if_end(s2)
+
+    g = _graph(body)
+    for last_masked, eos_last, expect in ((None, 0, 0), (B * L - 1, 0, 1), (B * L - 1, 1, 0),
+                                          (5 * L + 7, 0, 1)):
+        state.masked.zero_()
+        state.eos_hit.zero_()
+        if last_masked is not None:
+            state.masked[last_masked] = 1
+        state.eos_hit[B - 1] = eos_last
+        ran.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(ran.item()) == expect, (last_masked, eos_last)
+
+
 def test_capture_calls_outside_a_capture_are_rejected():
     w = synth.WORKLOADS["threshold_loop"].scaled(B=1, L=8, V=1024)
     gpu = GpuDecoder(w)
