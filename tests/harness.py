@@ -52,7 +52,7 @@ def _tracked_margins_ok(w, st: oracle.BlockState, lg: np.ndarray, s) -> bool:
             if a not in ids and not (ids == -1).any():
                 gained = [decay * st.cand_credit[b, i, k] + p_of(ids[k]) for k in range(K)]
                 g = np.sort(gained)
-                if g[1] - g[0] < EVICT_MARGIN * max(g[1], 1e-30):
+                if g.size > 1 and g[1] - g[0] < EVICT_MARGIN * max(g[1], 1e-30):
                     return False
             tid, tc = trial.cand_id[b, i], trial.cand_credit[b, i]
             sc = np.sort([p_of(tid[k]) * (1 + boost * np.log1p(tc[k]))
@@ -109,7 +109,7 @@ def margins_ok(w, st: oracle.BlockState, conf: np.ndarray, argmax: np.ndarray,
                 if argmax[b, i] in ids or (ids == -1).any():
                     continue
                 cr = np.sort(st.cand_credit[b, i])
-                if cr[1] - cr[0] < EVICT_MARGIN * max(cr[1], 1e-30):
+                if cr.size > 1 and cr[1] - cr[0] < EVICT_MARGIN * max(cr[1], 1e-30):
                     return False
     return True
 
