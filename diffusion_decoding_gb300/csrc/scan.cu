@@ -100,8 +100,12 @@ __global__ void __launch_bounds__(kScanThreads) read_rows_kernel(const uint8_t* 
 __global__ void __launch_bounds__(kScanThreads) kept_rows_map_kernel(
     const uint8_t* masked, const int32_t* eos_hit, int B, int L, int32_t* row_ids, int32_t* M,
     const int32_t* rows_read, const int32_t* count_read, int32_t* inv, int32_t* map) {
-  pdl_wait();
+  // The GEMM after this kernel reads only P and the row count (final once the commit kernel
+  // before this one started: that kernel waits for the statistics grid before it lets this one
+  // launch) until its epilogue, which waits for this grid; so it may launch at once and run its
+  // mainloop while the commit kernel and this one finish.
   pdl_trigger();
+  pdl_wait();  // the commit's block state
   const int R = B * L;
   int base = 0;
   for (int r0 = 0; r0 < R; r0 += kScanThreads) {

@@ -266,11 +266,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                           ? 1
                           : min(p.tail_tiles, m_pairs * p.n_tiles -
                                                   (pair - p.main_pairs) * p.tail_tiles);
-  // P, M and the row map come from the kernels before this one.  Every kernel of the step
-  // waits for its predecessor before it lets its dependents launch, so when this grid starts,
-  // the kernel two launches back has completed: with wait_late, P and M (written further back)
-  // are complete and only the row map (written by the kernel just before) is waited for, by
-  // the epilogue, while the mainloop overlaps that kernel.
+  // P, M and the row map come from the kernels before this one.  With wait_late (the
+  // single-read step), the kernel just before writes the row map and lets this grid launch
+  // before it waits for the commit kernel ahead of it; that commit kernel waited for the
+  // statistics grid before it let the map kernel launch, so P and M (written further back) are
+  // complete when this grid starts, and only the row map is waited for, by the epilogue, while
+  // the mainloop overlaps the commit and map kernels.
   if (!p.wait_late) pdl_wait();
   pdl_trigger();
   const int Mdev = *reinterpret_cast<const volatile int32_t*>(p.M);
