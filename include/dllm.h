@@ -18,8 +18,9 @@
  *
  * Conventions shared by every function:
  *  - Every pointer argument is DEVICE memory owned by the caller, except the `const dllm_*`
- *    descriptor structs themselves and `out_host` of dllm_get_status, which are host memory
- *    read (or written) before the function returns.  The library never allocates or frees
+ *    descriptor structs themselves, `out_host` of dllm_get_status and `handle_out` of
+ *    dllm_capture_condition, which are host memory read (or written) before the function
+ *    returns.  The library never allocates or frees
  *    device memory and never synchronises the stream, except dllm_get_status.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and runs
  *    asynchronously.  The functions hold no host state between calls, so a sequence of calls
