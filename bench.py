@@ -314,7 +314,6 @@ def run_smooth_step(args, rank, world, local):
     del E
     shape = dd.make_shape(B, L, V, dd.DLLM_BF16)
     state = dd.BlockState(B, L, device=dev)
-    fresh = dd.BlockState(B, L, device=dev)
     stats = dd.StatsBuffers(R, device=dev)
     ws = dd.workspace(dd.dllm_workspace_bytes(shape), dev)
     ws_s = dd.workspace(dd.dllm_smooth_workspace_bytes(shape, d), dev)
@@ -327,8 +326,8 @@ def run_smooth_step(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     def reset_state():
-        for name in ("masked", "tokens", "committed_now", "n_commit", "eos_hit"):
-            getattr(state, name).copy_(getattr(fresh, name), non_blocking=True)
+        # every step decodes a fresh block (every position masked): the library's reset kernel
+        dd.dllm_block_state_reset(state, credit=False)
 
     ev = {}
 
@@ -501,9 +500,9 @@ def run_smooth_step(args, rank, world, local):
     prob_gbs = prob_bytes / (prob_ms * 1e-3) / 1e9
     step_bytes = R * V * 2
     plan = dd.dllm_smooth_plan_info(shape, d)
-    # rows read, statistics + probabilities, commit, kept-row map, GEMM (+ split-K reduction),
-    # refresh
-    launches_per_step = 4 + (plan["launches"] - 2) + 1
+    # block reset, rows read, statistics + probabilities, commit, kept-row map, GEMM (+ split-K
+    # reduction), refresh
+    launches_per_step = 1 + 4 + (plan["launches"] - 2) + 1
     res = {
         "metric": METRIC,
         "value": world * B * 1e3 / ms,
