@@ -25,6 +25,8 @@ namespace dllm {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kStatsCtasPerSm = 4;  // resident statistics CTAs per SM (64 registers per thread)
+constexpr int kCompactRows = 4096;  // largest block the persistent statistics grid lists
 
 struct CommitCtx {
   int B, L;
@@ -36,6 +38,7 @@ struct FusedParams {
   const char* logits;
   int64_t row_stride_bytes;
   int V, S, chunk;
+  int compact;             // persistent grid over the rows read (listed in shared memory)
   int pdl_from;            // CTAs from this index on let the dependent commit grid launch
   const uint8_t* masked;   // rows to read (state.masked when committing)
   const int32_t* eos_hit;  // null in statistics-only mode
@@ -517,7 +520,31 @@ __device__ __forceinline__ void write_row_stats(const dllm_stats& st, int64_t r,
   st.argmax[r] = a.idx;
 }
 
+// One slice of row r (slice sl) reduced by the calling warp; lane 0 stores the result.
 template <int DT, bool kScalar>
+__device__ __forceinline__ void reduce_item(const FusedParams& p, int64_t r, int sl) {
+  const int64_t e0 = static_cast<int64_t>(sl) * p.chunk;
+  const int n = static_cast<int>(min(static_cast<int64_t>(p.V), e0 + p.chunk) - e0);
+  const char* row = p.logits + r * p.row_stride_bytes;
+  const RowAcc a = kScalar ? warp_reduce_slice_scalar<DT>(row, e0, n)
+                           : warp_reduce_slice<DT>(row, e0, n);
+  if ((threadIdx.x & 31) != 0) return;
+  if (p.S == 1) {  // the slice is the whole row
+    write_row_stats(p.stats, r, a);
+  } else {         // merged by the commit kernel
+    p.ws.part[r * p.S + sl] = make_uint4(__float_as_uint(a.m), __float_as_uint(a.s),
+                                         static_cast<uint32_t>(a.idx), 0u);
+  }
+}
+
+__device__ __forceinline__ void write_unread_stats(const dllm_stats& st, int64_t r) {
+  st.row_max[r] = -INFINITY;  // rows not read report -inf, -inf, 0, -1
+  st.lse[r] = -INFINITY;
+  st.conf[r] = 0.f;
+  st.argmax[r] = -1;
+}
+
+template <int DT, bool kScalar, bool kCompact>
 __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams p) {
   // the block state comes from the kernel before this one (the previous step's commit)
   pdl_wait();
@@ -525,34 +552,72 @@ __global__ void __launch_bounds__(kThreads, 4) stats_partials_kernel(FusedParams
   // CTAs count as triggered when they exit, so its CTAs do not hold SMs for the whole pass)
   if (static_cast<int>(blockIdx.x) >= p.pdl_from) pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp;
   const int S = p.S, L = p.c.L;
-  const int64_t n_items = static_cast<int64_t>(p.c.B) * L * S;
-  if (item >= n_items) return;
-  const int64_t r = item / S;
-  const int sl = static_cast<int>(item - r * S);
-  const bool active = (p.masked == nullptr || p.masked[r]) &&
-                      !(p.eos_hit != nullptr && p.eos_hit[r / L]);
-  if (!active) {  // rows not read report -inf, -inf, 0, -1 (written once, by slice 0's warp)
-    if (sl == 0 && lane == 0) {
-      p.stats.row_max[r] = -INFINITY;
-      p.stats.lse[r] = -INFINITY;
-      p.stats.conf[r] = 0.f;
-      p.stats.argmax[r] = -1;
+  const int64_t W = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp;
+  if constexpr (kCompact) {
+    extern __shared__ uint16_t act_rows[];  // the rows read, ascending
+    __shared__ int warp_cnt[kThreads / 32];
+    // Persistent grid over a block of at most kCompactRows rows: every CTA lists the rows read
+    // (masked, sequence running) in shared memory, and warp g of the grid reduces slices
+    // g, g + W, g + 2W, ... of the rows listed, so the work spreads evenly over the warps
+    // however many rows are read (CTA c writes the -inf statistics of the unread rows
+    // r = c mod grid).
+    // Thread t owns rows [t * per, (t + 1) * per): all its mask bytes (and the stop flags of
+    // the sequences they fall in) are loaded at once, then one block-wide scan of the counts
+    // places its rows read in the list.
+    const int R = p.c.B * L;
+    const int per = (R + kThreads - 1) / kThreads;  // <= kCompactRows / kThreads = 16
+    const int t0 = static_cast<int>(threadIdx.x) * per;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < kCompactRows / kThreads; ++k) {
+      const int r = t0 + k;
+      if (k < per && r < R) {
+        const bool a = (p.masked == nullptr || p.masked[r]) &&
+                       !(p.eos_hit != nullptr && p.eos_hit[r / L]);
+        if (a) bits |= 1u << k;
+        else if (r % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x))
+          write_unread_stats(p.stats, r);
+      }
     }
-    return;
-  }
-  const int64_t e0 = static_cast<int64_t>(sl) * p.chunk;
-  const int n = static_cast<int>(min(static_cast<int64_t>(p.V), e0 + p.chunk) - e0);
-  const char* row = p.logits + r * p.row_stride_bytes;
-  const RowAcc a = kScalar ? warp_reduce_slice_scalar<DT>(row, e0, n)
-                           : warp_reduce_slice<DT>(row, e0, n);
-  if (lane != 0) return;
-  if (S == 1) {  // the slice is the whole row
-    write_row_stats(p.stats, r, a);
-  } else {       // merged by the commit kernel
-    p.ws.part[item] = make_uint4(__float_as_uint(a.m), __float_as_uint(a.s),
-                                 static_cast<uint32_t>(a.idx), 0u);
+    const int cnt = __popc(bits);
+    int incl = cnt;  // inclusive scan of the counts over the warp, then over the warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_cnt[warp] = incl;
+    __syncthreads();
+    int off = incl - cnt, n_act = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      off += w < warp ? warp_cnt[w] : 0;
+      n_act += warp_cnt[w];
+    }
+    for (uint32_t b = bits; b != 0u; b &= b - 1u)
+      act_rows[off++] = static_cast<uint16_t>(t0 + __ffs(b) - 1);
+    __syncthreads();  // the list is complete
+    const int64_t n_items = static_cast<int64_t>(n_act) * S;
+    for (int64_t j = g; j < n_items; j += W) {
+      const int64_t k = j / S;
+      reduce_item<DT, kScalar>(p, act_rows[k], static_cast<int>(j - k * S));
+    }
+  } else {
+    // One item (row, slice) per warp: the grid covers every item.
+    (void)W;
+    const int64_t n_items = static_cast<int64_t>(p.c.B) * L * S;
+    if (g >= n_items) return;
+    const int64_t r = g / S;
+    const int sl = static_cast<int>(g - r * S);
+    const bool active = (p.masked == nullptr || p.masked[r]) &&
+                        !(p.eos_hit != nullptr && p.eos_hit[r / L]);
+    if (!active) {  // written once, by slice 0's warp
+      if (sl == 0 && lane == 0) write_unread_stats(p.stats, r);
+      return;
+    }
+    reduce_item<DT, kScalar>(p, r, sl);
   }
 }
 
@@ -763,21 +828,41 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
     p.eos_hit = state->eos_hit;
   }
   const int64_t items = static_cast<int64_t>(R) * p.S;
-  const dim3 grid1(static_cast<unsigned>((items + kThreads / 32 - 1) / (kThreads / 32)));
+  const int64_t ctas = (items + kThreads / 32 - 1) / (kThreads / 32);
+  // Blocks of up to kCompactRows rows that need more than one wave of CTAs run as a persistent
+  // grid (as many CTAs as fit at once) over the rows actually read; otherwise one warp per item.
+  const int64_t resident = static_cast<int64_t>(kStatsCtasPerSm) * std::max(1, sm_count);
+  p.compact = R <= kCompactRows && ctas > resident;
+  const dim3 grid1(static_cast<unsigned>(p.compact ? resident : ctas));
+  const size_t smem1 = p.compact ? sizeof(uint16_t) * static_cast<size_t>(R) : 0;
   p.pdl_from = std::max(0, static_cast<int>(grid1.x) - 2 * 4 * std::max(1, sm_count));
   // rows that are not all 16-byte aligned take the scalar-load reduction
   const bool scalar = (reinterpret_cast<uintptr_t>(logits) % 16) != 0 || p.row_stride_bytes % 16 != 0;
   cudaError_t e;
-  if (sh.dtype == DLLM_BF16)
-    e = scalar ? launch_dependent(stats_partials_kernel<DLLM_BF16, true>, grid1, dim3(kThreads), 0,
-                                  stream, p)
-               : launch_dependent(stats_partials_kernel<DLLM_BF16, false>, grid1, dim3(kThreads),
-                                  0, stream, p);
-  else
-    e = scalar ? launch_dependent(stats_partials_kernel<DLLM_F32, true>, grid1, dim3(kThreads), 0,
-                                  stream, p)
-               : launch_dependent(stats_partials_kernel<DLLM_F32, false>, grid1, dim3(kThreads),
-                                  0, stream, p);
+  const dim3 blk(kThreads);
+  if (sh.dtype == DLLM_BF16) {
+    if (p.compact)
+      e = scalar ? launch_dependent(stats_partials_kernel<DLLM_BF16, true, true>, grid1, blk,
+                                    smem1, stream, p)
+                 : launch_dependent(stats_partials_kernel<DLLM_BF16, false, true>, grid1, blk,
+                                    smem1, stream, p);
+    else
+      e = scalar ? launch_dependent(stats_partials_kernel<DLLM_BF16, true, false>, grid1, blk, 0,
+                                    stream, p)
+                 : launch_dependent(stats_partials_kernel<DLLM_BF16, false, false>, grid1, blk, 0,
+                                    stream, p);
+  } else {
+    if (p.compact)
+      e = scalar ? launch_dependent(stats_partials_kernel<DLLM_F32, true, true>, grid1, blk,
+                                    smem1, stream, p)
+                 : launch_dependent(stats_partials_kernel<DLLM_F32, false, true>, grid1, blk,
+                                    smem1, stream, p);
+    else
+      e = scalar ? launch_dependent(stats_partials_kernel<DLLM_F32, true, false>, grid1, blk, 0,
+                                    stream, p)
+                 : launch_dependent(stats_partials_kernel<DLLM_F32, false, false>, grid1, blk, 0,
+                                    stream, p);
+  }
   if (e != cudaSuccess) return e;
   if (ca.mode == kStatsOnly && p.S == 1) return cudaSuccess;
   // the merge (+ commit) kernel, one CTA per sequence, as a programmatic dependent launch

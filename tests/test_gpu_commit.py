@@ -131,6 +131,36 @@ def test_stats_ragged_sizes(V, dtype):
     assert close(stats.conf.cpu().numpy(), full.conf)
 
 
+@pytest.mark.parametrize("B,L,V,dtype,frac", [
+    (16, 64, 126464, "bf16", 0.3),   # 1024 rows: the persistent grid over the rows read
+    (8, 64, 126464, "bf16", 0.02),   # a nearly decided block
+    (8, 64, 126464, "bf16", 0.0),    # nothing read: every row reports -inf
+    (64, 64, 20001, "f32", 0.5),     # 4096 rows (the largest listed), fp32 rows read by scalar loads
+    (65, 64, 20000, "bf16", 0.5),    # 4160 rows: one warp per item again
+    (4, 256, 126464, "bf16", 1.0),   # every row read
+])
+def test_stats_over_partly_read_blocks(B, L, V, dtype, frac):
+    # statistics of the rows read, and -inf for the others, when the grid is persistent and
+    # its warps share out the rows read (blocks of up to 4096 rows that need more than one
+    # wave of CTAs), at and beyond its size limit
+    w = synth.WORKLOADS["threshold_loop"].scaled(B=B, L=L, V=V, dtype=dtype, eos_id=-1,
+                                                  plant="fixed")
+    lg = synth.logits(w, seed=B + L, it=1)
+    rng = np.random.default_rng(B * L)
+    masked = (rng.random(B * L) < frac).astype(np.uint8)
+    ref = oracle.stats(lg, masked)
+    stats = dd.StatsBuffers(B * L)
+    stats.argmax.fill_(12345)
+    shape = dd.make_shape(B, L, V, dd.DLLM_BF16 if dtype == "bf16" else dd.DLLM_F32)
+    ws = dd.workspace(dd.dllm_workspace_bytes(shape))
+    dd.dllm_decode_stats(to_device(lg), shape, torch.from_numpy(masked).cuda(), stats, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(stats.argmax.cpu().numpy(), ref.argmax)
+    assert close(stats.row_max.cpu().numpy(), ref.row_max, 0.0)
+    assert close(stats.lse.cpu().numpy(), ref.lse)
+    assert close(stats.conf.cpu().numpy(), ref.conf)
+
+
 def test_stats_padded_row_stride_and_ties():
     B, L, V, pad = 2, 3, 4000, 64
     rng = np.random.default_rng(1)
