@@ -829,10 +829,11 @@ cudaError_t launch_stats_commit(const void* logits, const dllm_shape& sh, const 
   }
   const int64_t items = static_cast<int64_t>(R) * p.S;
   const int64_t ctas = (items + kThreads / 32 - 1) / (kThreads / 32);
-  // Blocks of up to kCompactRows rows that need more than one wave of CTAs run as a persistent
-  // grid (as many CTAs as fit at once) over the rows actually read; otherwise one warp per item.
+  // Blocks of up to kCompactRows rows that need more than two waves of CTAs run as a persistent
+  // grid (as many CTAs as fit at once) over the rows actually read; otherwise one warp per item
+  // (with two waves or fewer there are few CTAs to launch, and the list costs ~1 us).
   const int64_t resident = static_cast<int64_t>(kStatsCtasPerSm) * std::max(1, sm_count);
-  p.compact = R <= kCompactRows && ctas > resident;
+  p.compact = R <= kCompactRows && ctas > 2 * resident;
   const dim3 grid1(static_cast<unsigned>(p.compact ? resident : ctas));
   const size_t smem1 = p.compact ? sizeof(uint16_t) * static_cast<size_t>(R) : 0;
   p.pdl_from = std::max(0, static_cast<int>(grid1.x) - 2 * 4 * std::max(1, sm_count));
