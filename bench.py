@@ -40,10 +40,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 # Decode loops stop on the device: a continue test every k iterations gates the rest of the
 # loop.  A test costs ~6-8 us of graph scheduling (a nested conditional section), so k trades
-# how soon a finished block stops against that cost: 2 for the threshold loop (its blocks end
-# within a few iterations), 8 where blocks decode for tens of iterations (1-2 % over a loop
-# without tests, measured).
-LOOP_TEST_EVERY = {"threshold_loop": 2}
+# how soon a finished block stops against that cost, about a quarter of the loop's expected
+# length: 2 for the threshold loop (its blocks end within a few iterations), 8 for the 24-step
+# credit loops, 16 for the hierarchical loops (up to 64 steps, nearly all of them decoding).
+LOOP_TEST_EVERY = {"threshold_loop": 2, "hierarchical_loop": 16, "hierarchical_levels_loop": 16}
 LOOP_TEST_EVERY_DEFAULT = 8
 
 
