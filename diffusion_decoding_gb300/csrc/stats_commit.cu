@@ -1,13 +1,16 @@
 // Softmax statistics + commit decision over one masked block (kernel "a": two launches).
 //
 // 1. stats_partials_kernel: every masked row of logits is streamed from HBM exactly once.  Rows
-//    are cut into 4 KB slices; each warp owns one slice, issues all of its 128-bit loads up
-//    front (8 per lane), takes the slice maximum with warp shuffles, sums exp(z - max) against
-//    that single maximum (no rescaling), finds the first index of the maximum, and writes one
-//    partial (max, sum, argmax).  Warps never wait for one another: no block barrier, no atomic,
-//    no fence.  (Completing each row inside this kernel, with an acquire/release atomic per
-//    slice on a row counter, cost ~17 us at 1024 rows x V = 126464: every warp's release fence
-//    waited behind the loads in flight.)
+//    are cut into 4 KB slices; a warp reduces one slice at a time: it issues all of its 128-bit
+//    loads up front (8 per lane), takes the slice maximum with warp shuffles, sums
+//    exp(z - max) against that single maximum (no rescaling), finds the first index of the
+//    maximum, and writes one partial (max, sum, argmax).  Small grids and blocks of more than
+//    4096 rows launch one warp per slice; other blocks run a persistent grid whose CTAs first
+//    list the rows read (one barrier-separated scan per CTA), so a nearly decided block does
+//    not launch a CTA per 8 slices that are not read.  No atomic, no fence.  (Completing each
+//    row inside this kernel, with an acquire/release atomic per slice on a row counter, cost
+//    ~17 us at 1024 rows x V = 126464: every warp's release fence waited behind the loads in
+//    flight.)
 // 2. commit_only_kernel (one CTA per sequence, chained with programmatic dependent launch so it
 //    is resident before the first kernel drains): merges the slice partials of its sequence's
 //    rows into their statistics (eight threads per row, every load issued up front), then runs
